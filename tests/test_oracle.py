@@ -1,0 +1,345 @@
+"""Pins for the fp64 CPU oracle, checked against things other than the oracle.
+
+Each test fixes a value by mathematics or by an independent routine: closed
+forms, exact rational arithmetic, brute-force search over every bf16 pattern,
+library routines (numpy / scipy / torch conversions) on cases that reduce to
+them, and the pages' worked chunking example.  None of them re-types the
+oracle's own loops.
+"""
+import bisect
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_bi_rmsnorm_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------- bf16 -------
+def _bf16_value(bits: int) -> float:
+    return struct.unpack("<f", struct.pack("<I", bits << 16))[0]
+
+
+# every finite non-negative bf16 value, ascending; 0x7f80 (inf) stands in as
+# 2^128 so the rounding boundary at the top of the range is searched too
+_ALL_POS = [_bf16_value(b) for b in range(0x7f80)] + [2.0 ** 128]
+
+
+def _nearest_bf16_bruteforce(v: float) -> int:
+    if math.isnan(v):
+        return 0x7fc0
+    sign = 0x8000 if math.copysign(1.0, v) < 0 else 0
+    a = abs(v)
+    if a >= 2.0 ** 128:
+        return sign | 0x7f80
+    i = bisect.bisect_left(_ALL_POS, a)
+    if i < len(_ALL_POS) and _ALL_POS[i] == a:
+        return sign | i
+    lo, hi = i - 1, i
+    dlo, dhi = a - _ALL_POS[lo], _ALL_POS[hi] - a
+    if dlo < dhi:
+        pick = lo
+    elif dhi < dlo:
+        pick = hi
+    else:
+        pick = lo if lo % 2 == 0 else hi
+    return sign | pick
+
+
+def _test_doubles(rng):
+    vals = [0.0, -0.0, 1.0, -1.0, 3.0, 1e-45, 2.0 ** -133, 2.0 ** -134,
+            2.0 ** -134 * 1.0000001, 2.0 ** -126, 2.0 ** -127 * 3,
+            3.3895313892515355e38, 3.3961e38, 2.0 ** 128 * (1 - 2 ** -9),
+            2.0 ** 128 * (1 - 2 ** -9) * (1 - 1e-16), 5e-324, 1e300, -1e-300]
+    # log-uniform magnitudes across (and beyond) the bf16 range
+    e = rng.uniform(-140, 129, size=4000)
+    m = rng.uniform(1, 2, size=4000)
+    s = rng.choice([-1.0, 1.0], size=4000)
+    vals += list(s * m * 2.0 ** e)
+    # exact midpoints between neighbours, and one double ulp either side
+    idx = rng.integers(0, 0x7f7f, size=2000)
+    for b in idx:
+        lo, hi = _bf16_value(int(b)), _bf16_value(int(b) + 1)
+        mid = (lo + hi) / 2  # exact in double
+        vals += [mid, np.nextafter(mid, 0.0), np.nextafter(mid, np.inf), -mid]
+    return np.array(vals, dtype=np.float64)
+
+
+def test_round_bf16_matches_bruteforce_nearest_even():
+    rng = np.random.default_rng(0)
+    vals = _test_doubles(rng)
+    got = oracle.round_bf16(vals)
+    want = np.array([_nearest_bf16_bruteforce(float(v)) for v in vals], dtype=np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(vals[i], hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def test_round_bf16_specials():
+    got = oracle.round_bf16(np.array([np.inf, -np.inf, np.nan, 0.0, -0.0]))
+    assert list(got[:2]) == [0x7f80, 0xff80]
+    assert (got[2] & 0x7f80) == 0x7f80 and (got[2] & 0x7f) != 0
+    assert list(got[3:]) == [0x0000, 0x8000]
+
+
+def test_round_bf16_agrees_with_ieee_float32_path():
+    # for values that are exactly float32, float32 -> bf16 (torch, IEEE RNE)
+    # rounds once and must agree
+    rng = np.random.default_rng(1)
+    f = (rng.standard_normal(20000) * 10.0 ** rng.uniform(-30, 30, 20000)).astype(np.float32)
+    got = oracle.round_bf16(f.astype(np.float64))
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_widening_is_exact_for_every_pattern():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.bf16_to_f64(pats)
+    want = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # sign of zero kept
+    assert math.copysign(1.0, got[0x8000]) == -1.0
+
+
+# ------------------------------------------------------------ RMSNorm -------
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_rmsnorm_constant_row_closed_form():
+    # x_j = c for all j: mean(x^2) = c^2, so y_j = w_j c / sqrt(c^2 + eps)
+    H, eps = 4096, 1e-6
+    w = inputs.rmsnorm_weight(H, seed=40)
+    for c in (1.0, -3.5, 0.0078125, 117.0):
+        x = torch.full((1, H), c, dtype=torch.bfloat16)
+        y = oracle.rmsnorm(x, w, eps)[0]
+        wv = w.double().numpy()
+        want = wv * c / math.sqrt(c * c + eps)
+        np.testing.assert_allclose(y, want, rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_one_hot_row_closed_form():
+    # x = c e_j: mean(x^2) = c^2 / H; only y_j is nonzero
+    H, eps, j, c = 512, 1e-6, 37, 2.5
+    w = inputs.rmsnorm_weight(H, seed=41)
+    x = torch.zeros(1, H, dtype=torch.bfloat16)
+    x[0, j] = c
+    y = oracle.rmsnorm(x, w, eps)[0]
+    want = float(w[j]) * c / math.sqrt(c * c / H + eps)
+    assert y[j] == pytest.approx(want, rel=1e-14)
+    assert np.count_nonzero(np.delete(y, j)) == 0
+
+
+def test_rmsnorm_zero_and_eps_dominated_rows():
+    H, eps = 256, 1e-6
+    w = torch.ones(H, dtype=torch.bfloat16)
+    y0 = oracle.rmsnorm(torch.zeros(1, H, dtype=torch.bfloat16), w, eps)
+    assert np.all(y0 == 0.0)
+    c = float(torch.tensor(1e-4, dtype=torch.bfloat16))  # c^2 = 1e-8 << eps
+    y = oracle.rmsnorm(torch.full((1, H), c, dtype=torch.bfloat16), w, eps)[0]
+    np.testing.assert_allclose(y, c / math.sqrt(c * c + eps), rtol=1e-14)
+
+
+def test_rmsnorm_power_of_two_scale_invariance_without_eps():
+    # with eps = 0, y(4x) = y(x) exactly: scaling by a power of two is exact
+    x = inputs.rmsnorm_rows(3, 1024, seed=42)
+    w = inputs.rmsnorm_weight(1024, seed=43)
+    y1 = oracle.rmsnorm(x, w, 0.0)
+    y4 = oracle.rmsnorm((x.float() * 4).to(torch.bfloat16), w, 0.0)
+    assert np.array_equal(y1, y4)
+
+
+def test_rmsnorm_general_rows_against_high_precision_decimal():
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    H, eps = 64, 1e-6
+    x = inputs.rmsnorm_rows(3, H, seed=44)
+    w = inputs.rmsnorm_weight(H, seed=45)
+    y = oracle.rmsnorm(x, w, eps)
+    xd = [[Decimal(float(v)) for v in row] for row in x.float().tolist()]
+    wd = [Decimal(float(v)) for v in w.float().tolist()]
+    for r in range(3):
+        ms = sum(v * v for v in xd[r]) / H + Decimal(eps)
+        inv = 1 / ms.sqrt()
+        want = [float(xd[r][i] * wd[i] * inv) for i in range(H)]
+        np.testing.assert_allclose(y[r], want, rtol=1e-14, atol=1e-300)
+
+
+def test_rmsnorm_rows_do_not_interact():
+    x = inputs.rmsnorm_rows(9, 768, seed=46)
+    w = inputs.rmsnorm_weight(768, seed=47)
+    full = oracle.rmsnorm(x, w, 1e-6)
+    for r in (0, 4, 8):
+        assert np.array_equal(full[r], oracle.rmsnorm(x[r:r + 1], w, 1e-6)[0])
+
+
+# --------------------------------------------------------------- GEMM -------
+def _exact_gemm(x: torch.Tensor, W: torch.Tensor):
+    xf = [[Fraction(float(v)) for v in row] for row in x.float().tolist()]
+    Wf = [[Fraction(float(v)) for v in row] for row in W.float().tolist()]
+    return [[sum(a * b for a, b in zip(xr, wr)) for wr in Wf] for xr in xf]
+
+
+@pytest.mark.parametrize("M,N,K", [(4, 8, 8), (3, 5, 7), (2, 9, 16)])
+def test_gemm_exact_rational_bruteforce(M, N, K):
+    x = inputs.gemm_rows(M, K, seed=50 + M)
+    W = (inputs.normal_bf16((N, K), seed=60 + N))
+    y = oracle.gemm(x, W)
+    exact = _exact_gemm(x, W)
+    absrow = oracle.gemm(x.abs(), W.abs())  # sum |x||w| bounds the rounding
+    for m in range(M):
+        for n in range(N):
+            err = abs(Fraction(float(y[m, n])) - exact[m][n])
+            assert err <= Fraction(K * 2.0 ** -52) * Fraction(float(absrow[m, n])) + Fraction(1, 10 ** 300)
+
+
+def test_gemm_identity_weight_returns_x():
+    K = 64
+    x = inputs.gemm_rows(5, K, seed=51)
+    I = torch.eye(K, dtype=torch.bfloat16)
+    assert np.array_equal(oracle.gemm(x, I), x.double().numpy())
+
+
+def test_gemm_matches_numpy_float64_matmul():
+    x = inputs.gemm_rows(33, 96, seed=52)
+    W = inputs.gemm_weight(80, 96, seed=53)
+    want = x.double().numpy() @ W.double().numpy().T
+    scale = np.abs(x.double().numpy()) @ np.abs(W.double().numpy()).T
+    assert np.all(np.abs(oracle.gemm(x, W) - want) <= 1e-13 * scale)
+
+
+def test_gemm_entries_equal_full_gemm():
+    x = inputs.gemm_rows(17, 128, seed=54)
+    W = inputs.gemm_weight(40, 128, seed=55)
+    full = oracle.gemm(x, W)
+    rng = np.random.default_rng(2)
+    ms, ns = rng.integers(0, 17, 100), rng.integers(0, 40, 100)
+    assert np.array_equal(oracle.gemm_entries(x, W, ms, ns), full[ms, ns])
+
+
+# ---------------------------------------------------------- attention -------
+def _problem(lens, Hq=8, Hkv=2, D=128, seed=70, spare=3):
+    return inputs.decode_problem(len(lens), Hq=Hq, Hkv=Hkv, D=D, seq_lens=lens,
+                                 seed=seed, spare_pages=spare)
+
+
+def test_attention_single_key_returns_v0():
+    p = _problem([1, 1, 1])
+    out = oracle.decode_attention(**p)
+    bt, v = p["block_table"], p["v_cache"].double().numpy()
+    for s in range(3):
+        for i in range(8):
+            np.testing.assert_array_equal(out[s, i], v[bt[s, 0], i // 4, 0])
+
+
+def test_attention_equal_keys_return_mean_of_values():
+    p = _problem([37, 300])
+    p["k_cache"][:] = p["k_cache"][0, 0, 0]  # every key identical
+    out = oracle.decode_attention(**p)
+    v = p["v_cache"].double().numpy()
+    bt = p["block_table"].numpy()
+    for s, L in enumerate([37, 300]):
+        for i in range(8):
+            rows = [v[bt[s, t // 16], i // 4, t % 16] for t in range(L)]
+            want = [float(sum(Fraction(float(r[d])) for r in rows) / L) for d in range(128)]
+            np.testing.assert_allclose(out[s, i], want, rtol=1e-13, atol=1e-15)
+
+
+def test_attention_two_keys_sigmoid_fixes_scale():
+    # q = a e0, k_t = b_t e0: scores s_t = a b_t / sqrt(D); the weights are
+    # p0 = 1 / (1 + exp(s1 - s0)), p1 = 1 - p0
+    D = 128
+    p = _problem([2], Hq=4, Hkv=1, D=D, spare=0)
+    a, b0, b1 = 3.0, 2.0, -1.5
+    p["q"][:] = 0
+    p["q"][0, :, 0] = a
+    p["k_cache"][:] = 0
+    pg = int(p["block_table"][0, 0])
+    p["k_cache"][pg, 0, 0, 0] = b0
+    p["k_cache"][pg, 0, 1, 0] = b1
+    out = oracle.decode_attention(**p)
+    s0, s1 = a * b0 / math.sqrt(D), a * b1 / math.sqrt(D)
+    p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    v = p["v_cache"].double().numpy()
+    want = p0 * v[pg, 0, 0] + (1 - p0) * v[pg, 0, 1]
+    for i in range(4):
+        np.testing.assert_allclose(out[0, i], want, rtol=1e-13, atol=1e-15)
+
+
+def test_attention_gqa_head_mapping():
+    # V of kv-head g is the constant g + 1, so query head i must output
+    # i // (Hq / Hkv) + 1 whatever the scores are
+    p = _problem([50, 7], Hq=8, Hkv=4)
+    for g in range(4):
+        p["v_cache"][:, g] = g + 1
+    out = oracle.decode_attention(**p)
+    for i in range(8):
+        np.testing.assert_allclose(out[:, i], i // 2 + 1, rtol=1e-14)
+
+
+def test_attention_matches_dense_scipy_softmax_of_gathered_pages():
+    from scipy.special import softmax
+    lens = [1, 15, 16, 17, 100, 257]
+    p = _problem(lens, spare=5)
+    p["k_cache"][~torch.isin(torch.arange(p["k_cache"].shape[0]),
+                             p["block_table"][p["block_table"] >= 0])] = 1000.0
+    out = oracle.decode_attention(**p)
+    q = p["q"].double().numpy()
+    k, v = p["k_cache"].double().numpy(), p["v_cache"].double().numpy()
+    bt = p["block_table"].numpy()
+    for s, L in enumerate(lens):
+        tok_pages, slots = bt[s, np.arange(L) // 16], np.arange(L) % 16
+        for i in range(8):
+            K = k[tok_pages, i // 4, slots]
+            V = v[tok_pages, i // 4, slots]
+            w = softmax(K @ q[s, i] / math.sqrt(128))
+            np.testing.assert_allclose(out[s, i], w @ V, rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("lens", [[1, 255, 256, 257], [1000, 513, 8192 // 8]])
+def test_chunked_method_equals_unchunked_definition(lens):
+    p = _problem(lens)
+    plain = oracle.decode_attention(**p)
+    chunked = oracle.decode_attention_chunked(**p, chunk=256)
+    np.testing.assert_allclose(chunked, plain, rtol=1e-12, atol=1e-14)
+
+
+def _golden_chunk_plans():
+    plans = []
+    with open(os.path.join(GOLDEN, "chunk_plan.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, tail = line.split(":")
+            L, chunk = (int(t) for t in head.split())
+            plans.append((L, chunk, [int(t) for t in tail.split()]))
+    return plans
+
+
+@pytest.mark.parametrize("L,chunk,plan", _golden_chunk_plans())
+def test_chunked_partials_follow_pages_chunk_plan(L, chunk, plan):
+    # with every key equal, each chunk's sum of exponentials l_c is exactly
+    # its token count, so the partials reveal the chunk lengths
+    p = _problem([L], Hq=4, Hkv=1)
+    p["k_cache"][:] = p["k_cache"][0, 0, 0]
+    _, part = oracle.decode_attention_chunked(**p, chunk=chunk, max_chunks=len(plan) + 2,
+                                              want_partials=True)
+    l = part[0, 0, :, 1]
+    assert list(l[:len(plan)]) == [float(n) for n in plan]
+    assert np.isnan(l[len(plan):]).all()
+
+
+def test_attention_rejects_empty_sequence():
+    p = _problem([4, 5])
+    p["seq_lens"] = torch.tensor([4, 0], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        oracle.decode_attention(**p)
