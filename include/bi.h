@@ -1,0 +1,183 @@
+/*
+ * bi.h -- batch-invariant forward kernels for LLM inference on GB300 (sm_103a).
+ *
+ * C ABI of libbi.so.  Every entry point takes plain device pointers, sizes and
+ * a CUDA stream; none allocates memory, keeps per-call state, or synchronises
+ * the stream (except bi_get_device_error).  All launches are asynchronous on
+ * `stream`.  Arguments are validated on the host before anything is launched:
+ * an invalid call returns an error status and launches nothing.
+ *
+ * The property every kernel here guarantees ("batch invariance", after
+ * "Defeating Nondeterminism in LLM Inference: The Core Role of Batch
+ * Invariance", section "Batch Invariance: The True Culprit"): the bits of one
+ * request's output depend only on that request's own inputs -- never on the
+ * batch size, the request's row position in the batch, the other requests in
+ * the batch, or (for attention) how many more tokens the KV cache holds
+ * beyond the request's own length.  Each output's floating-point reduction
+ * order is a fixed function of the problem's static sizes (hidden, K, D) and,
+ * for attention, of the request's own KV length.
+ *
+ * Data types: all activations, weights, caches and outputs are bf16
+ * (IEEE binary32 truncated to its top 16 bits); arithmetic is fp32; every
+ * output is rounded once, to nearest-even, to bf16.
+ */
+#ifndef BI_H_
+#define BI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BI_ABI_VERSION 1
+
+/* Tokens per KV-cache page and per attention split.  Both are fixed: the
+ * split size is part of the arithmetic (see bi_decode_attention). */
+#define BI_PAGE_SIZE 16
+#define BI_DECODE_CHUNK 256
+
+typedef enum {
+    BI_OK = 0,
+    BI_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad eps ... */
+    BI_ERR_UNSUPPORTED_SHAPE = 2,  /* a size this build does not handle */
+    BI_ERR_MISALIGNED = 3,         /* pointer or leading dimension not 16-byte aligned */
+    BI_ERR_WORKSPACE_TOO_SMALL = 4,
+    BI_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+    BI_ERR_DEVICE_TIMEOUT = 6,     /* a kernel gave up waiting on a barrier */
+    BI_ERR_DEVICE_BAD_INPUT = 7    /* a kernel found an invalid device-resident
+                                      input (seq_lens / block_table entry) */
+} bi_status;
+
+/* BI_ABI_VERSION of the loaded library. */
+int bi_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char* bi_status_string(bi_status s);
+
+/* Synchronise `stream`, then read and clear the current device's error word.
+ * Kernels that detect a problem on the device (a barrier wait that ran past
+ * its limit, a sequence length or page index out of range) record the first
+ * such event there and stop work on the affected output instead of faulting.
+ * Returns BI_OK, BI_ERR_DEVICE_TIMEOUT, BI_ERR_DEVICE_BAD_INPUT or BI_ERR_CUDA. */
+bi_status bi_get_device_error(cudaStream_t stream);
+
+/*
+ * bi_rmsnorm -- y[r][i] = bf16( x[r][i] * rsqrt(mean_j x[r][j]^2 + eps) * w[i] )
+ *
+ * Operation: RMSNorm as in "Defeating Nondeterminism in LLM Inference: The
+ * Core Role of Batch Invariance", section "1. Batch-Invariant RMSNorm": each
+ * row is reduced entirely by one CTA ("data-parallel RMSNorm"); no split
+ * reduction is used at any batch size.  The sum of squares is accumulated in
+ * fp32 in an order that depends only on `hidden`.
+ *
+ *   x      device, bf16 [rows][ld_x], row-major; only the first `hidden`
+ *          elements of each row are read.
+ *   w      device, bf16 [hidden].
+ *   y      device, bf16 [rows][ld_y]; may alias x when ld_y == ld_x.
+ *   rows   0 .. 2^31-1 (0 launches nothing).
+ *   hidden multiple of 8, 8 .. 32768.
+ *   ld_x, ld_y  in elements, >= hidden, multiples of 8 (16-byte rows).
+ *   eps    finite, >= 0.
+ * Pointers must be 16-byte aligned.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * MISALIGNED, CUDA.
+ */
+bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int32_t hidden,
+                     int64_t ld_x, int64_t ld_y, float eps, cudaStream_t stream);
+
+/*
+ * bi_gemm -- y[M][N] = bf16( x[M][K] . W[N][K]^T ), fp32 accumulation.
+ *
+ * Operation: "2. Batch-Invariant Matrix Multiplication" of the same page: a
+ * data-parallel tiled matmul with ONE kernel configuration for every shape --
+ * a fixed 128x256 output tile, K walked in ascending 64-wide blocks, each
+ * block as four ascending 16-deep tcgen05 MMAs accumulating in TMEM.  No
+ * split-K or stream-K for any M, and the same MMA instruction shape always.
+ *
+ *   x  device, bf16 [M][ld_x] row-major (K contiguous).
+ *   W  device, bf16 [N][ld_w] row-major: the nn.Linear weight layout.
+ *   y  device, bf16 [M][ld_y] row-major; must not overlap x or W.
+ *   M  0 .. 2^31-1;  N, K  >= 8 and multiples of 8.
+ *   ld_x, ld_w, ld_y  in elements, multiples of 8, >= K, >= K, >= N.
+ * Pointers must be 16-byte aligned.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * MISALIGNED, CUDA.
+ */
+bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, int32_t N, int32_t K,
+                  int64_t ld_x, int64_t ld_w, int64_t ld_y, cudaStream_t stream);
+
+/*
+ * Workspace bytes bi_decode_attention needs for B sequences of at most
+ * max_seq_len tokens with Hq query heads of size D: one fp32 partial
+ * (max, sum, D-vector) per (sequence, query head, 256-token chunk).
+ * Returns 0 for invalid arguments.
+ */
+size_t bi_decode_attention_workspace_size(int32_t B, int32_t Hq, int32_t D, int32_t max_seq_len);
+
+/* Number of 256-token chunks a sequence of `seq_len` tokens is cut into
+ * (ceil(seq_len / 256)), and the length of chunk c (256 for all but the last).
+ * 0 for invalid arguments. */
+int32_t bi_decode_num_chunks(int32_t seq_len);
+int32_t bi_decode_chunk_len(int32_t seq_len, int32_t c);
+
+/*
+ * bi_decode_attention -- one query row per sequence attends over that
+ * sequence's paged KV cache:
+ *     out[s][i] = softmax_t( scale * q[s][i] . k_t[g] ) . v_t[g],
+ *     g = i / (Hq / Hkv),  t = 0 .. seq_lens[s]-1.
+ *
+ * Operation: "3. Batch-Invariant Attention" of the same page, with the fixed
+ * split-SIZE strategy ("Fixed Size Split KV Strategy"; "Batch Invariance and
+ * Numerical Reproducibility": 1000 tokens = 3 x 256 + 232).  Each sequence's
+ * keys are cut into consecutive 256-token chunks; one CTA computes each
+ * chunk's partial (running max, sum of exponentials, unnormalised output)
+ * with an online softmax over its 16 pages in a fixed order; the partials are
+ * then folded in ascending chunk order with the log-sum-exp rule.  The
+ * arithmetic for a sequence depends only on its own length and data, never on
+ * B, on other sequences, or on tokens stored past seq_lens[s].  The cache is
+ * read only: the caller writes the current token's K/V into its page slot
+ * BEFORE calling (one K/V layout for cached and new tokens).
+ *
+ *   q            device, bf16 [B][Hq][D].
+ *   k_cache,
+ *   v_cache      device, bf16 [num_pages][Hkv][page_size][D]: each
+ *                (page, kv-head) is one contiguous page_size x D block.
+ *   block_table  device, int32 [B][max_pages_per_seq]: page index of each
+ *                sequence's token block t / page_size.  Entries past a
+ *                sequence's last page are never read.
+ *   seq_lens     device, int32 [B]: 1 .. max_seq_len tokens per sequence.
+ *   B            0 .. 65535 sequences (0 launches nothing).
+ *   Hq, Hkv      query and key/value heads; Hq % Hkv == 0, Hq / Hkv <= 8.
+ *   D            128.   page_size  16.
+ *   num_pages    pages in each cache; num_pages * Hkv * page_size < 2^31.
+ *   max_seq_len  upper bound on every seq_lens entry, >= 1 and
+ *                <= max_pages_per_seq * page_size; it sizes the launch grid.
+ *   scale        softmax scale (1/sqrt(D) for standard attention), finite, > 0.
+ *   out          device, bf16 [B][Hq][D].
+ *   workspace    device, >= bi_decode_attention_workspace_size(B, Hq, D,
+ *                max_seq_len) bytes, 16-byte aligned; may be null when that
+ *                size is 0.  After the call it holds, for every sequence with
+ *                more than one chunk, the fp32 chunk partials in the layout
+ *                [B][Hq][chunks][D] (unnormalised outputs) followed by
+ *                [B][Hq][chunks][2] (max in log2 units of scale*q.k, sum).
+ * Pointers to bf16 data must be 16-byte aligned, int32 arrays 4-byte aligned.
+ * Host-side errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED,
+ * WORKSPACE_TOO_SMALL, CUDA.  A seq_lens entry outside 1 .. max_seq_len or a
+ * block_table entry outside 0 .. num_pages-1 is found on the device: the
+ * affected sequence's output is left unwritten and bi_get_device_error
+ * reports BI_ERR_DEVICE_BAD_INPUT.
+ */
+bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, int32_t max_pages_per_seq,
+                              const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv,
+                              int32_t D, int32_t page_size, int32_t num_pages,
+                              int32_t max_seq_len, float scale, void* out, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BI_H_ */

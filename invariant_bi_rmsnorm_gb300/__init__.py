@@ -1,1 +1,178 @@
-"""Batch-invariant forward kernels for LLM inference on GB300 (sm_103a)."""
+"""Batch-invariant forward kernels for LLM inference on GB300 (sm_103a).
+
+Thin Python binding over libbi.so (C ABI: include/bi.h).  Each function only
+checks and marshals its torch arguments (device pointers, sizes, leading
+dimensions, the current CUDA stream) and calls the library; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback:
+tensors must live on a CUDA device, and a missing library raises.
+
+    rmsnorm(x, w, eps)                    y = x * rsqrt(mean(x^2) + eps) * w, per row
+    gemm(x, W)                            y = x @ W.T  (W in nn.Linear [N, K] layout)
+    decode_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_len)
+                                          paged decode attention, 256-token splits
+
+Every output row's bits depend only on that row's own inputs (batch
+invariance); see include/bi.h for the exact contract of each call.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+from ._lib import DECODE_CHUNK, PAGE_SIZE
+
+__all__ = ["BiError", "rmsnorm", "gemm", "decode_attention", "decode_attention_workspace_size",
+           "decode_num_chunks", "decode_chunk_len", "get_device_error", "abi_version",
+           "status_string", "PAGE_SIZE", "DECODE_CHUNK"]
+
+
+class BiError(RuntimeError):
+    """A libbi.so call returned a status other than BI_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def status_string(status: int) -> str:
+    return _lib.load().bi_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(_lib.load().bi_abi_version())
+
+
+def _check(status: int, where: str) -> None:
+    if status != _lib.BI_OK:
+        raise BiError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _cuda_bf16(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+
+
+def _row_major_2d(t: torch.Tensor, name: str) -> int:
+    """Leading dimension (elements) of a 2-D tensor with unit inner stride."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    return int(t.stride(0)) if t.shape[0] > 1 else int(t.shape[1])
+
+
+def get_device_error(stream=None) -> None:
+    """Synchronise `stream` and raise BiError if a kernel recorded a
+    device-side problem (a barrier wait past its limit, or an out-of-range
+    seq_lens / block_table entry).  Clears the record."""
+    _check(_lib.load().bi_get_device_error(_stream(stream)), "bi_get_device_error")
+
+
+# ------------------------------------------------------------- RMSNorm ------
+def rmsnorm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, out: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """Batch-invariant RMSNorm over the last dimension of x [rows, hidden]."""
+    _cuda_bf16(x, "x")
+    _cuda_bf16(w, "w")
+    if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1] or not w.is_contiguous():
+        raise ValueError("rmsnorm: x [rows, hidden] and contiguous w [hidden] expected")
+    rows, hidden = x.shape
+    if out is None:
+        out = torch.empty((rows, hidden), dtype=torch.bfloat16, device=x.device)
+    _cuda_bf16(out, "out")
+    if tuple(out.shape) != (rows, hidden):
+        raise ValueError("rmsnorm: out has the wrong shape")
+    ld_x = _row_major_2d(x, "x")
+    ld_y = _row_major_2d(out, "out")
+    _check(_lib.load().bi_rmsnorm(x.data_ptr(), w.data_ptr(), out.data_ptr(), rows, hidden,
+                                  ld_x, ld_y, float(eps), _stream(stream)), "bi_rmsnorm")
+    return out
+
+
+# ---------------------------------------------------------------- GEMM ------
+def gemm(x: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """Batch-invariant y = x @ W.T with x [M, K] and W [N, K] (nn.Linear layout)."""
+    _cuda_bf16(x, "x")
+    _cuda_bf16(W, "W")
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1]:
+        raise ValueError("gemm: x [M, K] and W [N, K] expected")
+    M, K = x.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda_bf16(out, "out")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("gemm: out has the wrong shape")
+    _check(_lib.load().bi_gemm(x.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K,
+                               _row_major_2d(x, "x"), _row_major_2d(W, "W"),
+                               _row_major_2d(out, "out"), _stream(stream)), "bi_gemm")
+    return out
+
+
+# ----------------------------------------------------------- attention ------
+def decode_attention_workspace_size(B: int, Hq: int, D: int, max_seq_len: int) -> int:
+    return int(_lib.load().bi_decode_attention_workspace_size(B, Hq, D, max_seq_len))
+
+
+def decode_num_chunks(seq_len: int) -> int:
+    return int(_lib.load().bi_decode_num_chunks(seq_len))
+
+
+def decode_chunk_len(seq_len: int, c: int) -> int:
+    return int(_lib.load().bi_decode_chunk_len(seq_len, c))
+
+
+def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                     scale: float | None = None, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Batch-invariant paged decode attention.
+
+    q [B, Hq, D]; k_cache, v_cache [num_pages, Hkv, 16, D]; block_table
+    [B, max_pages_per_seq] int32; seq_lens [B] int32 (1 .. max_seq_len).
+    `max_seq_len` is a host-side bound on seq_lens that sizes the launch (it
+    is not read from the device, so no synchronisation happens)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _cuda_bf16(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens")):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("decode_attention: q [B,Hq,D] and caches [P,Hkv,page,D] expected")
+    B, Hq, D = q.shape
+    num_pages, Hkv, page, D2 = k_cache.shape
+    if D2 != D or block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("decode_attention: inconsistent shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _cuda_bf16(out, "out")
+    if tuple(out.shape) != (B, Hq, D) or not out.is_contiguous():
+        raise ValueError("decode_attention: out must be a contiguous [B, Hq, D] tensor")
+    need = decode_attention_workspace_size(B, Hq, D, max_seq_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.load().bi_decode_attention(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+        block_table.shape[1], seq_lens.data_ptr(), B, Hq, Hkv, D, page, num_pages,
+        int(max_seq_len), float(scale), out.data_ptr(), ws_ptr, ws_bytes, _stream(stream)),
+        "bi_decode_attention")
+    return out

@@ -1,0 +1,123 @@
+// Library-wide pieces of the C ABI: status strings, the device error word and
+// the TMA descriptor encoder shared by the kernels.
+#include <mutex>
+
+#include "bi_internal.h"
+
+namespace {
+
+// One error word per device.  Kernels record the first device-side problem
+// here (see bi_get_device_error); it is a flag, not part of any arithmetic.
+__device__ uint32_t g_bi_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+}  // namespace
+
+namespace bi {
+
+uint32_t* device_error_word() {
+    int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bi_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+int sm_count() {
+    int dev = current_device();
+    if (dev < 0) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner_elems,
+                              uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                              uint32_t box_outer) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q{};
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return CUDA_ERROR_NOT_FOUND;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+    }
+    cuuint64_t dims[2] = {inner_elems, outer_rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace bi
+
+extern "C" {
+
+int bi_abi_version(void) { return BI_ABI_VERSION; }
+
+const char* bi_status_string(bi_status s) {
+    switch (s) {
+        case BI_OK: return "BI_OK";
+        case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG";
+        case BI_ERR_UNSUPPORTED_SHAPE: return "BI_ERR_UNSUPPORTED_SHAPE";
+        case BI_ERR_MISALIGNED: return "BI_ERR_MISALIGNED";
+        case BI_ERR_WORKSPACE_TOO_SMALL: return "BI_ERR_WORKSPACE_TOO_SMALL";
+        case BI_ERR_CUDA: return "BI_ERR_CUDA";
+        case BI_ERR_DEVICE_TIMEOUT: return "BI_ERR_DEVICE_TIMEOUT";
+        case BI_ERR_DEVICE_BAD_INPUT: return "BI_ERR_DEVICE_BAD_INPUT";
+    }
+    return "BI_ERR_UNKNOWN";
+}
+
+bi_status bi_get_device_error(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return BI_ERR_CUDA;
+    uint32_t* p = bi::device_error_word();
+    if (!p) return BI_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return BI_ERR_CUDA;
+    if (v != 0) {
+        uint32_t zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return BI_ERR_CUDA;
+    }
+    switch (v & 0xffu) {
+        case 0: return BI_OK;
+        case BI_ERR_DEVICE_TIMEOUT: return BI_ERR_DEVICE_TIMEOUT;
+        case BI_ERR_DEVICE_BAD_INPUT: return BI_ERR_DEVICE_BAD_INPUT;
+    }
+    return BI_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cstdint>
+
+#include <cuda.h>  // CUtensorMap and its enums only; libcuda is not linked
+#include <cuda_runtime.h>
+
+#include "bi.h"
+
+namespace bi {
+
+// Limits of every bounded barrier wait: about two seconds of wall clock
+// (a healthy wait lasts microseconds), and a poll count as a backstop in case
+// the clock does not advance.
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kWaitPollLimit = 1u << 28;
+
+// Device error word values (low byte = bi_status, next byte = where).
+enum : uint32_t {
+    kErrTimeout = BI_ERR_DEVICE_TIMEOUT,
+    kErrBadInput = BI_ERR_DEVICE_BAD_INPUT,
+};
+enum : uint32_t {
+    kWhereRmsnorm = 1u << 8,
+    kWhereGemmProducer = 2u << 8,
+    kWhereGemmMma = 3u << 8,
+    kWhereGemmEpilogue = 4u << 8,
+    kWhereAttnSplit = 5u << 8,
+    kWhereAttnMerge = 6u << 8,
+};
+
+// Device address of the current device's error word (nullptr on failure).
+uint32_t* device_error_word();
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point
+// so the library does not link libcuda.  Returns CUDA_SUCCESS or an error.
+CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner_elems,
+                              uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                              uint32_t box_outer);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace bi

@@ -1,0 +1,444 @@
+// bi_decode_attention: paged decode attention with fixed-size KV splits.
+//
+// "Defeating Nondeterminism in LLM Inference: The Core Role of Batch
+// Invariance", section "3. Batch-Invariant Attention" (figures "Fixed Number
+// Split KV Strategy" / "Fixed Size Split KV Strategy") and "Batch Invariance
+// and Numerical Reproducibility" (a 1,000-token cache = three 256-token
+// chunks plus one of 232): decode has too few query rows to fill the GPU, so
+// the KV sequence is split -- but by a fixed split SIZE, so the reduction
+// order of a sequence depends only on its own length.
+//
+// Kernel 1 (split): one CTA per (sequence s, kv-head g, chunk c).  The chunk
+// is tokens [256c, min(256c + 256, L)), i.e. up to 16 pages of 16 tokens.
+// Warp w (of 4) owns the chunk's pages w, w+4, w+8, w+12 and runs an online
+// softmax over them in that order, for the Hq/Hkv query heads that share
+// kv-head g.  Pages arrive by TMA (2-D tiled loads, 128-byte swizzle) into a
+// 2-stage ring per warp.  Per page:
+//     S^T[16 tok x 8 heads] = K_page[16 x 128] . Q^T[128 x 8]   (8 mma.sync)
+//     p = exp2(S * scale * log2 e - m_new), rounded to bf16
+//     O^T[128 x 8] = O^T * alpha + V^T[128 x 16] . P^T[16 x 8]   (8 mma.sync)
+// The four warp states are then folded in warp order 0..3.  A sequence with
+// one chunk is normalised and written here; otherwise the chunk partial
+// (m, l, O) goes to the workspace.
+// Kernel 2 (merge): for each (sequence, query head) with more than one chunk,
+// fold the partials in ascending chunk order with the log-sum-exp rule and
+// write bf16(O / l).
+//
+// Tokens past the sequence end inside its last page are masked to -inf and
+// their V rows are zeroed in shared memory before use, so whatever the cache
+// holds there (a later token, or uninitialised bits) never reaches the result.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kPage = BI_PAGE_SIZE;             // 16 tokens
+constexpr int kChunk = BI_DECODE_CHUNK;         // 256 tokens
+constexpr int kPagesPerChunk = kChunk / kPage;  // 16
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStagesPerWarp = 2;
+constexpr int kStages = kWarps * kStagesPerWarp;
+constexpr int kHalfBytes = kPage * 64 * 2;         // 16 rows x 64 dims: one TMA box
+constexpr int kMatBytes = 2 * kHalfBytes;          // one (page, kv-head) K or V block
+constexpr int kStageBytes = 2 * kMatBytes;         // K + V
+constexpr int kMaxGroup = 8;                       // query heads per kv-head (mma N)
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*bars, pages*/;
+
+static_assert(kStages * kStageBytes >= kWarps * (2 * kMaxGroup + kMaxGroup * kD) * 4,
+              "combine area must fit in the stage ring");
+
+// Byte offset of the 16-byte chunk `ch` (0..15) of row `r` (0..15) inside one
+// K or V page block as laid down by two 16x64 TMA boxes with 128-byte
+// swizzle: the box for dims [64*(ch/8), +64) starts at (ch/8)*2048, each row
+// is 128 bytes, and the 16-byte unit index is XORed with (row % 8).
+__device__ __forceinline__ uint32_t swz(int r, int ch) {
+    return static_cast<uint32_t>((ch >> 3) * kHalfBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+struct SplitArgs {
+    const __nv_bfloat16* q;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    __nv_bfloat16* out;
+    float* ws_acc;  // [B][Hq][max_chunks][D]
+    float* ws_ml;   // [B][Hq][max_chunks][2]
+    uint32_t* err;
+    int max_pages_per_seq;
+    int Hq, Hkv, group;
+    int num_pages;
+    int max_seq_len;
+    int max_chunks;
+    float scale_log2;  // scale * log2(e)
+};
+
+__global__ void __launch_bounds__(kThreads)
+    attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+    const int c = blockIdx.x;
+    const int g = blockIdx.y;
+    const int s = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    const int L = a.seq_lens[s];
+    if (L < 1 || L > a.max_seq_len) {
+        if (tid == 0 && c == 0 && g == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+        return;
+    }
+    const int nch = (L + kChunk - 1) / kChunk;
+    if (c >= nch) return;
+    const int t0 = c * kChunk;
+    const int ntok = min(kChunk, L - t0);
+    const int npages = (ntok + kPage - 1) / kPage;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    int32_t* rows_s = reinterpret_cast<int32_t*>(bars + kStages);  // TMA row of each page
+    __shared__ int bad_page;
+
+    if (tid == 0) {
+        bad_page = 0;
+        for (int i = 0; i < kStages; ++i) bi::mbar_init(&bars[i], 1);
+        bi::fence_mbar_init();
+        bi::tma_prefetch_desc(&tmap_k);
+        bi::tma_prefetch_desc(&tmap_v);
+    }
+    __syncthreads();
+    if (tid < npages) {
+        const int pg = a.block_table[static_cast<int64_t>(s) * a.max_pages_per_seq + c * kPagesPerChunk + tid];
+        if (pg < 0 || pg >= a.num_pages) {
+            bad_page = 1;
+        } else {
+            rows_s[tid] = (pg * a.Hkv + g) * kPage;
+        }
+    }
+    __syncthreads();
+    if (bad_page) {
+        if (tid == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+        return;
+    }
+
+    auto stage_ptr = [&](int st) { return smem + st * kStageBytes; };
+    auto issue = [&](int j) {  // warp-local page j -> stage warp*2 + (j & 1)
+        const int p = warp + kWarps * j;
+        const int st = warp * kStagesPerWarp + (j & 1);
+        uint8_t* kd = stage_ptr(st);
+        uint8_t* vd = kd + kMatBytes;
+        const int row = rows_s[p];
+        bi::mbar_arrive_expect_tx(&bars[st], kStageBytes);
+        bi::tma_load_2d(kd, &tmap_k, &bars[st], 0, row);
+        bi::tma_load_2d(kd + kHalfBytes, &tmap_k, &bars[st], 64, row);
+        bi::tma_load_2d(vd, &tmap_v, &bars[st], 0, row);
+        bi::tma_load_2d(vd + kHalfBytes, &tmap_v, &bars[st], 64, row);
+    };
+
+    const int my_pages = (npages > warp) ? (npages - warp + kWarps - 1) / kWarps : 0;
+    if (lane == 0) {
+        for (int j = 0; j < my_pages && j < kStagesPerWarp; ++j) issue(j);
+    }
+
+    // Q^T as the mma B operand: lane holds head (lane/4) of the group and
+    // dims 16ks + 2(lane%4) + {0,1} (b0) and +8 (b1).
+    const int qh = lane >> 2;
+    uint32_t qb0[8], qb1[8];
+    {
+        const bool valid = qh < a.group;
+        const __nv_bfloat16* qp =
+            a.q + (static_cast<int64_t>(s) * a.Hq + g * a.group + (valid ? qh : 0)) * kD + 2 * (lane & 3);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            qb0[ks] = valid ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks) : 0u;
+            qb1[ks] = valid ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8) : 0u;
+        }
+    }
+
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float acc[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+    // ldmatrix lane roles
+    const int lm_j = lane >> 3;        // which 8x8 matrix this lane addresses
+    const int lm_r = lane & 7;         // row within it
+    int timed_out_at = -1;
+
+    for (int j = 0; j < my_pages; ++j) {
+        const int p = warp + kWarps * j;
+        const int st = warp * kStagesPerWarp + (j & 1);
+        if (!bi::mbar_wait(&bars[st], (j >> 1) & 1)) {
+            timed_out_at = j;
+            break;
+        }
+        const uint32_t ks_base = bi::smem_u32(stage_ptr(st));
+        const uint32_t vs_base = ks_base + kMatBytes;
+        const int valid = min(kPage, ntok - p * kPage);
+        if (valid < kPage) {
+            // zero V rows past the sequence end (16-byte units)
+            uint8_t* vd = stage_ptr(st) + kMatBytes;
+            for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
+                const int r = valid + (idx >> 4), ch = idx & 15;
+                *reinterpret_cast<uint4*>(vd + swz(r, ch)) = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+
+        // S^T = K . Q^T  (tokens on M, heads on N), dims in ascending 16-blocks
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            const int r = lm_r + 8 * (lm_j & 1);
+            const int ch = 2 * ks + (lm_j >> 1);
+            bi::ldmatrix_x4(ks_base + swz(r, ch), a0, a1, a2, a3);
+            bi::mma_bf16_16816(sc, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+        }
+        // sc[0], sc[1]: token lane/4, heads 2(lane%4)+{0,1}; sc[2], sc[3]: token +8
+        const int tokA = lane >> 2, tokB = tokA + 8;
+        const float x0 = tokA < valid ? sc[0] * a.scale_log2 : -INFINITY;
+        const float x1 = tokA < valid ? sc[1] * a.scale_log2 : -INFINITY;
+        const float x2 = tokB < valid ? sc[2] * a.scale_log2 : -INFINITY;
+        const float x3 = tokB < valid ? sc[3] * a.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+        const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+        const uint32_t pA = bi::pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
+        const uint32_t pB = bi::pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
+        // the row sums use the same bf16-rounded weights that multiply V
+        float ps0 = __uint_as_float(pA << 16) + __uint_as_float(pB << 16);
+        float ps1 = __uint_as_float(pA & 0xffff0000u) + __uint_as_float(pB & 0xffff0000u);
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) {
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+        }
+        l_run[0] = __fmaf_rn(l_run[0], al0, ps0);
+        l_run[1] = __fmaf_rn(l_run[1], al1, ps1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+        }
+        // P^T fragments (tokens on K, heads on N) by an in-register transpose
+        const uint32_t pb0 = bi::movmatrix_trans(pA);
+        const uint32_t pb1 = bi::movmatrix_trans(pB);
+        // O^T += V^T . P^T, dims in ascending 16-blocks
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            const int r = lm_r + 8 * (lm_j >> 1);
+            const int ch = 2 * mt + (lm_j & 1);
+            bi::ldmatrix_x4_trans(vs_base + swz(r, ch), a0, a1, a2, a3);
+            bi::mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+        // hand the stage back to TMA for this warp's page j + 2
+        bi::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && j + kStagesPerWarp < my_pages) issue(j + kStagesPerWarp);
+    }
+    if (timed_out_at >= 0 && lane == 0) {
+        bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+        // give this warp's copies still in flight (pages j and j + 1) one more
+        // bounded chance to land before the CTA's shared memory is released
+        for (int j = timed_out_at; j < my_pages && j < timed_out_at + kStagesPerWarp; ++j)
+            (void)bi::mbar_wait(&bars[warp * kStagesPerWarp + (j & 1)], (j >> 1) & 1);
+    }
+    __syncthreads();  // every warp done with the ring: reuse it for the fold
+
+    // per-warp state -> shared: m[8], l[8], acc[8 heads][128 dims]
+    float* wst = reinterpret_cast<float*>(smem) + warp * (2 * kMaxGroup + kMaxGroup * kD);
+    const int h0 = 2 * (lane & 3);
+    if (lane < 4) {
+        wst[h0] = m_run[0];
+        wst[h0 + 1] = m_run[1];
+        wst[kMaxGroup + h0] = l_run[0];
+        wst[kMaxGroup + h0 + 1] = l_run[1];
+    }
+    float* wacc = wst + 2 * kMaxGroup;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int d = 16 * mt + (lane >> 2);
+        wacc[h0 * kD + d] = acc[mt][0];
+        wacc[(h0 + 1) * kD + d] = acc[mt][1];
+        wacc[h0 * kD + d + 8] = acc[mt][2];
+        wacc[(h0 + 1) * kD + d + 8] = acc[mt][3];
+    }
+    __syncthreads();
+
+    // fold warps 0..3 in order; thread = output dim
+    const int d = tid;
+    const float* st0 = reinterpret_cast<const float*>(smem);
+    constexpr int kWarpStride = 2 * kMaxGroup + kMaxGroup * kD;
+    for (int h = 0; h < a.group; ++h) {
+        float M = st0[h];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, st0[w * kWarpStride + h]);
+        float Ls = 0.f, A = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float* ws = st0 + w * kWarpStride;
+            const float f = exp2f(ws[h] - M);
+            Ls = __fmaf_rn(ws[kMaxGroup + h], f, Ls);
+            A = __fmaf_rn(ws[2 * kMaxGroup + h * kD + d], f, A);
+        }
+        const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
+        if (nch == 1) {
+            a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(A, Ls));
+        } else {
+            const int64_t pidx = row * a.max_chunks + c;
+            a.ws_acc[pidx * kD + d] = A;
+            if (d == 0) {
+                a.ws_ml[pidx * 2] = M;
+                a.ws_ml[pidx * 2 + 1] = Ls;
+            }
+        }
+    }
+}
+
+// Fold the chunk partials of one (sequence, query head) in ascending chunk
+// order:  M' = max(M, m_c);  l' = l 2^(M-M') + l_c 2^(m_c-M');
+//         O' = O 2^(M-M') + O_c 2^(m_c-M');   out = bf16(O / l).
+__global__ void __launch_bounds__(kD)
+    attn_merge_kernel(const int32_t* __restrict__ seq_lens, const float* __restrict__ ws_acc,
+                      const float* __restrict__ ws_ml, __nv_bfloat16* __restrict__ out, int Hq,
+                      int max_chunks, int max_seq_len) {
+    const int hq = blockIdx.x;
+    const int s = blockIdx.y;
+    const int d = threadIdx.x;
+    const int L = seq_lens[s];
+    if (L < 1 || L > max_seq_len) return;  // reported by the split kernel
+    const int nch = (L + kChunk - 1) / kChunk;
+    if (nch < 2) return;
+    const int64_t base = (static_cast<int64_t>(s) * Hq + hq) * max_chunks;
+    float M = ws_ml[base * 2];
+    float Ls = ws_ml[base * 2 + 1];
+    float A = ws_acc[base * kD + d];
+    for (int c = 1; c < nch; ++c) {
+        const float mc = ws_ml[(base + c) * 2];
+        const float lc = ws_ml[(base + c) * 2 + 1];
+        const float ac = ws_acc[(base + c) * kD + d];
+        const float Mn = fmaxf(M, mc);
+        const float fo = exp2f(M - Mn), fc = exp2f(mc - Mn);
+        Ls = __fmaf_rn(lc, fc, __fmul_rn(Ls, fo));
+        A = __fmaf_rn(ac, fc, __fmul_rn(A, fo));
+        M = Mn;
+    }
+    out[(static_cast<int64_t>(s) * Hq + hq) * kD + d] = __float2bfloat16_rn(__fdiv_rn(A, Ls));
+}
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+bool g_attr_set[64] = {};
+
+}  // namespace
+
+extern "C" size_t bi_decode_attention_workspace_size(int32_t B, int32_t Hq, int32_t D,
+                                                     int32_t max_seq_len) {
+    if (B < 0 || Hq <= 0 || D <= 0 || max_seq_len < 1) return 0;
+    const int64_t chunks = ceil_div(max_seq_len, kChunk);
+    if (chunks < 2) return 0;
+    return static_cast<size_t>(B) * Hq * chunks * (static_cast<size_t>(D) + 2) * sizeof(float);
+}
+
+extern "C" int32_t bi_decode_num_chunks(int32_t seq_len) {
+    return seq_len < 1 ? 0 : ceil_div(seq_len, kChunk);
+}
+
+extern "C" int32_t bi_decode_chunk_len(int32_t seq_len, int32_t c) {
+    const int32_t n = bi_decode_num_chunks(seq_len);
+    if (c < 0 || c >= n) return 0;
+    return c < n - 1 ? kChunk : seq_len - (n - 1) * kChunk;
+}
+
+extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, int32_t max_pages_per_seq,
+                                         const int32_t* seq_lens, int32_t B, int32_t Hq,
+                                         int32_t Hkv, int32_t D, int32_t page_size,
+                                         int32_t num_pages, int32_t max_seq_len, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_pages_per_seq < 1 || num_pages < 1 ||
+        max_seq_len < 1)
+        return BI_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return BI_ERR_INVALID_ARG;
+    if (D != kD || page_size != kPage) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (Hq % Hkv != 0 || Hq / Hkv > kMaxGroup) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (B > 65535) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(num_pages) * Hkv * kPage >= (int64_t{1} << 31))
+        return BI_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages_per_seq) * kPage)
+        return BI_ERR_INVALID_ARG;
+    if (B == 0) return BI_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return BI_ERR_INVALID_ARG;
+    if (!bi::aligned16(q) || !bi::aligned16(k_cache) || !bi::aligned16(v_cache) ||
+        !bi::aligned16(out) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3))
+        return BI_ERR_MISALIGNED;
+    const int max_chunks = ceil_div(max_seq_len, kChunk);
+    const size_t need = bi_decode_attention_workspace_size(B, Hq, D, max_seq_len);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return BI_ERR_WORKSPACE_TOO_SMALL;
+        if (!bi::aligned16(workspace)) return BI_ERR_MISALIGNED;
+    }
+
+    CUtensorMap tk, tv;
+    const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv * kPage;
+    if (bi::encode_tensor_map_2d(&tk, k_cache, kD, rows, kD * 2, 64, kPage) != CUDA_SUCCESS ||
+        bi::encode_tensor_map_2d(&tv, v_cache, kD, rows, kD * 2, 64, kPage) != CUDA_SUCCESS)
+        return BI_ERR_CUDA;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BI_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+        if (cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            return BI_ERR_CUDA;
+        g_attr_set[dev] = true;
+    }
+
+    SplitArgs args;
+    args.q = static_cast<const __nv_bfloat16*>(q);
+    args.block_table = block_table;
+    args.seq_lens = seq_lens;
+    args.out = static_cast<__nv_bfloat16*>(out);
+    args.ws_acc = need ? static_cast<float*>(workspace) : nullptr;
+    args.ws_ml = need ? static_cast<float*>(workspace) +
+                            static_cast<size_t>(B) * Hq * max_chunks * kD
+                      : nullptr;
+    args.err = bi::device_error_word();
+    args.max_pages_per_seq = max_pages_per_seq;
+    args.Hq = Hq;
+    args.Hkv = Hkv;
+    args.group = Hq / Hkv;
+    args.num_pages = num_pages;
+    args.max_seq_len = max_seq_len;
+    args.max_chunks = max_chunks;
+    args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+    attn_split_kernel<<<dim3(max_chunks, Hkv, B), kThreads, kSmemBytes, stream>>>(tk, tv, args);
+    if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
+    if (max_chunks >= 2) {
+        attn_merge_kernel<<<dim3(Hq, B), kD, 0, stream>>>(seq_lens, args.ws_acc, args.ws_ml,
+                                                          args.out, Hq, max_chunks, max_seq_len);
+        if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
+    }
+    return BI_OK;
+}

@@ -1,0 +1,257 @@
+// bi_gemm: y[M,N] = x[M,K] . W[N,K]^T on tcgen05 tensor cores, one kernel
+// configuration for every shape.
+//
+// "Defeating Nondeterminism in LLM Inference: The Core Role of Batch
+// Invariance", section "2. Batch-Invariant Matrix Multiplication": a
+// data-parallel matmul gives each output tile to one core and reduces its
+// whole K range there; splitting K when M*N is small, or switching tensor-core
+// instruction or tile shape with the batch size, changes the reduction order.
+// So this kernel has exactly one tile shape (128 x 256), one MMA instruction
+// shape (tcgen05.mma kind::f16, M=128, N=256, K=16) and one K order (64-wide
+// blocks ascending, each as 4 ascending 16-deep MMAs into one fp32 TMEM
+// accumulator), whatever M, N and K are.  No split-K, no stream-K.
+//
+// Structure (persistent, one CTA per SM, warp-specialised):
+//   warp 0      TMA producer: x and W tiles (128x64 and 256x64 bf16, 128-byte
+//               swizzle) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//               issues the MMAs from one thread;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4) ..), fp32 -> bf16 round-to-nearest-even, store.
+// Rows past M and columns past N read as zeros (TMA out-of-bounds fill) and
+// are never stored; adding zero products leaves the other sums unchanged.
+#include <cuda_bf16.h>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;  // 16 KiB
+constexpr int kBBytes = BN * BK * 2;  // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;  // 2 x 256 fp32 columns
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9
+// = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
+// bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major tile stored as 128-byte rows
+// with the 128-byte swizzle: start address >> 4 (bits 0-13), leading byte
+// offset (unused for this layout, bits 16-29), stride byte offset = 1024 bytes
+// between 8-row groups (bits 32-45), the fixed 0b001 at bits 46-48, swizzle
+// mode 2 = 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (uint64_t{1} << 16) |
+           (uint64_t{1024 >> 4} << 32) | (uint64_t{1} << 46) | (uint64_t{2} << 61);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                        const __grid_constant__ CUtensorMap tmap_w, __nv_bfloat16* __restrict__ y,
+                        int M, int N, int K, int64_t ld_y, uint32_t* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;
+    uint64_t* tempty = tfull + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_m = (M + BM - 1) / BM;
+    const int num_n = (N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            bi::mbar_init(&full[i], 1);
+            bi::mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            bi::mbar_init(&tfull[i], 1);
+            bi::mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
+        }
+        bi::fence_mbar_init();
+        bi::tma_prefetch_desc(&tmap_x);
+        bi::tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 1) {
+        bi::tmem_alloc(tmem_slot, kTmemCols);
+        bi::tmem_relinquish();
+    }
+    bi::tc_fence_before();
+    __syncthreads();
+    bi::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                const int mb = tile % num_m, nb = tile / num_m;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!bi::mbar_wait(&empty[stage], phase ^ 1)) {
+                        bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmProducer);
+                        goto producer_done;
+                    }
+                    uint8_t* sa = smem + stage * kStageBytes;
+                    bi::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    bi::tma_load_2d(sa, &tmap_x, &full[stage], kb * BK, mb * BM);
+                    bi::tma_load_2d(sa + kABytes, &tmap_w, &full[stage], kb * BK, nb * BN);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                if (!bi::mbar_wait(&tempty[acc], acc_phase ^ 1)) {
+                    bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmMma);
+                    break;
+                }
+                bi::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!bi::mbar_wait(&full[stage], phase)) {
+                        bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmMma);
+                        ok = false;
+                        break;
+                    }
+                    bi::tc_fence_after();
+                    const uint32_t sa = bi::smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        bi::tc_mma_f16(d_tmem, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k),
+                                       kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    bi::tc_commit(&empty[stage]);  // stage free once these MMAs finish
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                bi::tc_commit(&tfull[acc]);  // accumulator ready for the epilogue
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+        }
+    } else {
+        // epilogue warps 2..5 -> TMEM lane quarter warp % 4
+        const int quarter = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int mb = tile % num_m, nb = tile / num_m;
+            if (!bi::mbar_wait(&tfull[acc], acc_phase)) {
+                if (lane == 0) bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmEpilogue);
+                break;
+            }
+            bi::tc_fence_after();
+            const int row = mb * BM + quarter * 32 + lane;
+            __nv_bfloat16* yrow = y + static_cast<int64_t>(row) * ld_y;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                const int col0 = nb * BN + ch * 32;
+                if (col0 >= N) break;  // warp-uniform
+                uint32_t r[32];
+                bi::tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                bi::tmem_ld_wait();
+                if (row < M) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (col0 + 8 * v + 8 > N) break;
+                        uint4 o;
+                        o.x = bi::pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                        o.y = bi::pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                        o.z = bi::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                        o.w = bi::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                        *reinterpret_cast<uint4*>(yrow + col0 + 8 * v) = o;
+                    }
+                }
+            }
+            bi::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bi::mbar_arrive(&tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    bi::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        bi::tc_fence_after();
+        bi::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+bool g_attr_set[64] = {};
+
+}  // namespace
+
+extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, int32_t N,
+                             int32_t K, int64_t ld_x, int64_t ld_w, int64_t ld_y,
+                             cudaStream_t stream) {
+    if (M < 0 || N < 8 || K < 8) return M < 0 ? BI_ERR_INVALID_ARG : BI_ERR_UNSUPPORTED_SHAPE;
+    if ((N & 7) || (K & 7)) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (ld_x < K || ld_w < K || ld_y < N) return BI_ERR_INVALID_ARG;
+    if ((ld_x & 7) || (ld_w & 7) || (ld_y & 7)) return BI_ERR_MISALIGNED;
+    if (M == 0) return BI_OK;
+    if (!x || !W || !y) return BI_ERR_INVALID_ARG;
+    if (!bi::aligned16(x) || !bi::aligned16(W) || !bi::aligned16(y)) return BI_ERR_MISALIGNED;
+
+    CUtensorMap tx, tw;
+    if (bi::encode_tensor_map_2d(&tx, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                                 static_cast<uint64_t>(ld_x) * 2, BK, BM) != CUDA_SUCCESS ||
+        bi::encode_tensor_map_2d(&tw, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                                 static_cast<uint64_t>(ld_w) * 2, BK, BN) != CUDA_SUCCESS)
+        return BI_ERR_CUDA;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BI_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+        if (cudaFuncSetAttribute(gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            return BI_ERR_CUDA;
+        g_attr_set[dev] = true;
+    }
+    const int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (tiles > 0x7fffffffLL) return BI_ERR_UNSUPPORTED_SHAPE;
+    const int sms = bi::sm_count();
+    if (sms <= 0) return BI_ERR_CUDA;
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    gemm_tcgen05_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
+        tx, tw, static_cast<__nv_bfloat16*>(y), M, N, K, ld_y, bi::device_error_word());
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}

@@ -1,0 +1,124 @@
+// bi_rmsnorm: data-parallel RMSNorm, one row per CTA.
+//
+// "Defeating Nondeterminism in LLM Inference: The Core Role of Batch
+// Invariance", section "1. Batch-Invariant RMSNorm": keeping each row's whole
+// reduction inside one core makes its order independent of the batch size;
+// splitting one row over several cores at small batch would change it, so
+// that is never done here.
+//
+// Reduction order (a function of `hidden` only):
+//   1. thread t owns the 16-byte vectors t, t+T, t+2T, ... of the row
+//      (T = threads per CTA); it sums x^2 over its vectors in that order,
+//      each vector's 8 elements left to right, with fused multiply-adds;
+//   2. each warp folds its 32 partials with an xor butterfly (16,8,4,2,1) and
+//      lane 0's result is taken;
+//   3. every thread folds the per-warp sums in warp order 0, 1, 2, ...
+// Then r = rsqrt(sum / hidden + eps) and y = bf16_rn((x * r) * w) in fp32.
+#include <cuda_bf16.h>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace {
+
+constexpr int kMaxThreads = 512;
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+template <int VPT>
+__global__ void __launch_bounds__(kMaxThreads)
+    rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloat16* __restrict__ w, __nv_bfloat16* y,
+                   int hidden, int64_t ld_x, int64_t ld_y, float eps) {
+    __shared__ float warp_sums[kMaxThreads / 32];
+    const int nvec = hidden >> 3;
+    const int tid = threadIdx.x;
+    const int T = blockDim.x;
+    const int64_t row = blockIdx.x;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * ld_x);
+    const uint4* wr = reinterpret_cast<const uint4*>(w);
+
+    uint4 xv[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + j * T;
+        xv[j] = (v < nvec) ? __ldcs(xr + v) : make_uint4(0, 0, 0, 0);
+    }
+
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const uint32_t u[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = bf16_lo(u[e]), b = bf16_hi(u[e]);
+            s = __fmaf_rn(a, a, s);
+            s = __fmaf_rn(b, b, s);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((tid & 31) == 0) warp_sums[tid >> 5] = s;
+    __syncthreads();
+    const int nwarps = T >> 5;
+    float total = warp_sums[0];
+    for (int i = 1; i < nwarps; ++i) total += warp_sums[i];
+    const float r = rsqrtf(__fdiv_rn(total, static_cast<float>(hidden)) + eps);
+
+    uint4* yr = reinterpret_cast<uint4*>(y + row * ld_y);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + j * T;
+        if (v >= nvec) continue;
+        const uint4 wv = __ldg(wr + v);
+        const uint32_t xu[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = __fmul_rn(__fmul_rn(bf16_lo(xu[e]), r), bf16_lo(wu[e]));
+            const float b = __fmul_rn(__fmul_rn(bf16_hi(xu[e]), r), bf16_hi(wu[e]));
+            o[e] = bi::pack_bf16x2(a, b);
+        }
+        yr[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+}  // namespace
+
+extern "C" bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t rows,
+                                int32_t hidden, int64_t ld_x, int64_t ld_y, float eps,
+                                cudaStream_t stream) {
+    if (rows < 0 || rows > 0x7fffffffLL) return BI_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || eps != eps || eps > 3.0e38f) return BI_ERR_INVALID_ARG;
+    if (hidden < 8 || hidden > 32768 || (hidden & 7)) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (ld_x < hidden || ld_y < hidden) return BI_ERR_INVALID_ARG;
+    if ((ld_x & 7) || (ld_y & 7)) return BI_ERR_MISALIGNED;
+    if (rows == 0) return BI_OK;
+    if (!x || !w || !y) return BI_ERR_INVALID_ARG;
+    if (!bi::aligned16(x) || !bi::aligned16(w) || !bi::aligned16(y)) return BI_ERR_MISALIGNED;
+
+    // Thread count and vectors per thread depend on `hidden` alone.
+    const int nvec = hidden / 8;
+    int threads, vpt;
+    if (nvec <= kMaxThreads) {
+        threads = (nvec + 31) / 32 * 32;
+        vpt = 1;
+    } else {
+        threads = kMaxThreads;
+        vpt = (nvec + kMaxThreads - 1) / kMaxThreads;
+    }
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const auto* wb = static_cast<const __nv_bfloat16*>(w);
+    auto* yb = static_cast<__nv_bfloat16*>(y);
+    const dim3 grid(static_cast<unsigned>(rows));
+    if (vpt == 1)
+        rmsnorm_kernel<1><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+    else if (vpt == 2)
+        rmsnorm_kernel<2><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+    else if (vpt <= 4)
+        rmsnorm_kernel<4><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+    else
+        rmsnorm_kernel<8><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}

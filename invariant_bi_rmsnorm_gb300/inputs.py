@@ -112,10 +112,12 @@ def decode_problem(B: int, Hq: int = 32, Hkv: int = 8, D: int = 128,
     v_cache, block_table, seq_lens (CPU tensors)."""
     if seq_lens is None:
         seq_lens = seq_lens_uniform(B, max_len, seed=seed + 1)
+        width = (max_len + page_size - 1) // page_size  # room for any length <= max_len
     else:
         seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32)
+        width = None
     bt, num_pages = paged_layout(seq_lens, seed=seed + 2, page_size=page_size,
-                                 spare_pages=spare_pages)
+                                 spare_pages=spare_pages, max_pages_per_seq=width)
     k, v = kv_cache(num_pages, Hkv, D, seed=seed + 3, page_size=page_size)
     q = decode_queries(len(seq_lens), Hq, D, seed=seed + 4)
     return {"q": q, "k_cache": k, "v_cache": v, "block_table": bt,

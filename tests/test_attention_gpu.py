@@ -1,0 +1,242 @@
+"""bi_decode_attention on the GPU: parity with the fp64 oracle and bitwise
+invariance to batch composition, position and KV-cache growth.
+
+Tolerances: the stated one, max|gpu - ref| <= 1e-2 * max|ref| per call, and a
+tighter per-row one, max over d of |gpu - ref| <= 2^-6 * max_d |ref| + 2^-12,
+derived from the arithmetic (bf16-rounded softmax weights, relative error
+2^-9 each, averaged over the row; one bf16 rounding of the output).  A
+dropped, repeated or mis-masked token moves a short row far beyond it.
+
+Workload (GQA 32 query / 8 kv heads, head_dim 128, bf16 cache, 16-token pages,
+q/k/v ~ N(0, 1), lengths uniform on [1, 8192], pages scattered by a seeded
+permutation).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import invariant_bi_rmsnorm_gb300 as bi
+import oracle
+from invariant_bi_rmsnorm_gb300 import inputs
+from tests._util import bits, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _to_dev(p):
+    return {k: v.cuda() for k, v in p.items()}
+
+
+def _run(p, max_seq_len=None, **kw):
+    d = _to_dev(p)
+    if max_seq_len is None:
+        max_seq_len = int(p["seq_lens"].max())
+    return bi.decode_attention(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                               d["seq_lens"], max_seq_len=max_seq_len, **kw)
+
+
+def _check(out, ref):
+    got = f64(out)
+    err = np.abs(got - ref)
+    assert err.max() <= 1e-2 * np.abs(ref).max(), f"call tolerance: {err.max()}"
+    row_tol = 2.0 ** -6 * np.abs(ref).max(axis=-1) + 2.0 ** -12
+    row_err = err.max(axis=-1)
+    bad = row_err > row_tol
+    assert not bad.any(), f"{bad.sum()} rows beyond tolerance, first {np.argwhere(bad)[0]}"
+
+
+EDGE_LENS = [1, 2, 15, 16, 17, 31, 255, 256, 257, 511, 512, 513, 1000, 4097, 8192]
+
+
+def test_edge_lengths_against_oracle():
+    p = inputs.decode_problem(len(EDGE_LENS), seq_lens=EDGE_LENS, seed=200, spare_pages=7)
+    _check(_run(p), oracle.decode_attention(**p))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4), (32, 8), (64, 8), (24, 8)])
+def test_gqa_group_sizes(Hq, Hkv):
+    lens = [3, 300, 1000]
+    p = inputs.decode_problem(3, Hq=Hq, Hkv=Hkv, seq_lens=lens, seed=210 + Hq)
+    _check(_run(p), oracle.decode_attention(**p))
+
+
+def test_custom_scale():
+    p = inputs.decode_problem(4, seq_lens=[5, 70, 600, 2000], seed=220)
+    _check(_run(p, scale=0.03), oracle.decode_attention(**p, scale=0.03))
+
+
+def test_garbage_past_sequence_end_is_ignored():
+    # tokens past seq_len inside the last page hold NaN/inf: never read into
+    # the result (masked scores, zeroed V rows)
+    lens = [1, 17, 250, 1000]
+    p = inputs.decode_problem(4, seq_lens=lens, seed=230)
+    ref = oracle.decode_attention(**p)
+    clean = bits(_run(p))
+    bt = p["block_table"]
+    for s, L in enumerate(lens):
+        last = int(bt[s, (L - 1) // 16])
+        if L % 16:
+            p["k_cache"][last, :, L % 16:] = float("nan")
+            p["v_cache"][last, :, L % 16:] = float("inf")
+    dirty = _run(p)
+    assert np.array_equal(bits(dirty), clean)
+    _check(dirty, ref)
+
+
+def test_single_sequence_bit_identical_in_any_batch():
+    B = 128
+    p = inputs.decode_problem(B, max_len=8192, seed=240)
+    full = bits(_run(p, max_seq_len=8192))  # block tables have room for 8192
+    for s in (0, 5, 77, 127):
+        one = {k: (v[s:s + 1] if k in ("q", "block_table", "seq_lens") else v) for k, v in p.items()}
+        alone = bits(_run(one, max_seq_len=8192))
+        assert np.array_equal(alone[0], full[s]), f"sequence {s} alone differs from batched"
+        # a launch sized for a smaller bound (fewer grid chunks) gives the same bits
+        alone2 = bits(_run(one))
+        assert np.array_equal(alone2[0], full[s])
+    # permutation of the batch
+    perm = torch.randperm(B, generator=torch.Generator().manual_seed(5))
+    pp = dict(p)
+    for k in ("q", "block_table", "seq_lens"):
+        pp[k] = p[k][perm].contiguous()
+    assert np.array_equal(bits(_run(pp, max_seq_len=8192)), full[perm.numpy()])
+
+
+def test_growth_from_100_to_1000_tokens():
+    # One sequence grows from 100 to 1000 tokens: before each call the caller
+    # appends the new tokens' K/V into their page slots, and the batch
+    # partners change every step.  The outputs for two fixed queries taken at
+    # L = 100 and L = 512 are recorded when first computed, then recomputed
+    # once the cache holds all 1000 tokens (seq_len set back): same bits.
+    Hq, D = 32, 128
+    g = torch.Generator().manual_seed(250)
+    grown = inputs.decode_problem(1, seq_lens=[1000], seed=251)
+    partners = inputs.decode_problem(64, max_len=2000, seed=252)
+    num_pages_a = grown["k_cache"].shape[0]
+    k_true = torch.cat([grown["k_cache"], partners["k_cache"]])
+    v_true = torch.cat([grown["v_cache"], partners["v_cache"]])
+    pbt = partners["block_table"].clone()
+    pbt[pbt >= 0] += num_pages_a
+    width = 125  # room for 2000 tokens
+    gbt = grown["block_table"][0]
+
+    def table(rows):
+        t = torch.full((len(rows), width), -1, dtype=torch.int32)
+        for i, r in enumerate(rows):
+            t[i, :r.shape[0]] = r
+        return t
+
+    kd, vd = k_true.cuda(), v_true.cuda()
+    kd[:num_pages_a] = 0  # the growing sequence's pages start empty
+    vd[:num_pages_a] = 0
+
+    def append(t0, t1):  # write tokens [t0, t1) of the growing sequence
+        for t in range(t0, t1):
+            pg, slot = int(gbt[t // 16]), t % 16
+            kd[pg, :, slot] = k_true[pg, :, slot].cuda()
+            vd[pg, :, slot] = v_true[pg, :, slot].cuda()
+
+    q_fixed = {L: inputs.decode_queries(1, Hq, D, seed=1000 + L)[0] for L in (100, 512)}
+    recorded = {}
+    have = 0
+    for L in list(range(100, 1001, 4)):
+        append(have, L)
+        have = L
+        nb = int(torch.randint(0, 9, (1,), generator=g))
+        pick = torch.randperm(64, generator=g)[:nb].tolist()
+        pos = int(torch.randint(0, nb + 1, (1,), generator=g))
+        rows = [pbt[i] for i in pick]
+        lens = [int(partners["seq_lens"][i]) for i in pick]
+        qs = [partners["q"][i] for i in pick]
+        rows.insert(pos, gbt)
+        lens.insert(pos, L)
+        qs.insert(pos, q_fixed.get(L, inputs.decode_queries(1, Hq, D, seed=2000 + L)[0]))
+        out = bi.decode_attention(torch.stack(qs).cuda(), kd, vd, table(rows).cuda(),
+                                  torch.tensor(lens, dtype=torch.int32).cuda(), max_seq_len=2000)
+        if L in q_fixed:
+            recorded[L] = bits(out[pos])
+    assert have == 1000
+    for L, want in recorded.items():
+        out = bi.decode_attention(q_fixed[L][None].cuda(), kd, vd, table([gbt]).cuda(),
+                                  torch.tensor([L], dtype=torch.int32).cuda(), max_seq_len=1000)
+        assert np.array_equal(bits(out[0]), want), f"output at L={L} changed after growth"
+        one = {"q": q_fixed[L][None], "k_cache": k_true, "v_cache": v_true,
+               "block_table": table([gbt]), "seq_lens": torch.tensor([L], dtype=torch.int32)}
+        _check(out, oracle.decode_attention(**one))
+
+
+def test_complete_chunk_partials_stable_as_cache_grows():
+    # the workspace holds each chunk's (m, l, O) partial; a complete chunk's
+    # partial must not change when the sequence grows past it
+    Hq, D = 32, 128
+    base = inputs.decode_problem(1, seq_lens=[2048], seed=260)
+    max_chunks = 8
+    ws = torch.zeros(bi.decode_attention_workspace_size(1, Hq, D, 2048), dtype=torch.uint8,
+                     device="cuda")
+    acc_elems = 1 * Hq * max_chunks * D
+
+    def partial_acc(L):
+        p = dict(base)
+        p["seq_lens"] = torch.tensor([L], dtype=torch.int32)
+        ws.zero_()
+        _run(p, max_seq_len=2048, workspace=ws)
+        f = ws.view(torch.float32)
+        return (f[:acc_elems].view(Hq, max_chunks, D).cpu().numpy().copy(),
+                f[acc_elems:].view(Hq, max_chunks, 2).cpu().numpy().copy())
+
+    a1, m1 = partial_acc(600)   # chunks 0, 1 complete; chunk 2 partial
+    a2, m2 = partial_acc(2048)  # all 8 complete
+    assert np.array_equal(a1[:, :2].view(np.uint32), a2[:, :2].view(np.uint32))
+    assert np.array_equal(m1[:, :2].view(np.uint32), m2[:, :2].view(np.uint32))
+    # and they agree with the oracle's fp64 chunk partials: m is kept in log2
+    # units, so l and O are scaled by 2^(m) / e^(m_oracle)
+    _, part = oracle.decode_attention_chunked(**base, chunk=256, max_chunks=max_chunks,
+                                              want_partials=True)
+    for c in range(8):
+        mo, lo, ao = part[0, :, c, 0], part[0, :, c, 1], part[0, :, c, 2:]
+        factor = np.exp(mo - m2[:, c, 0].astype(np.float64) * math.log(2.0))
+        np.testing.assert_allclose(m2[:, c, 1], lo * factor, rtol=2 ** -7)
+        o_gpu = a2[:, c] / m2[:, c, 1:2]
+        o_ref = ao / lo[:, None]
+        assert (np.abs(o_gpu - o_ref).max(axis=-1) <= 2 ** -6 * np.abs(o_ref).max(axis=-1) + 2 ** -12).all()
+
+
+def test_c4_full_size_sampled_parity():
+    # batch 256, lengths U[1, 8192]: 32 sampled sequences checked against the
+    # oracle, and every row of the launch is finite
+    for B in (1, 16, 128, 256):
+        p = inputs.decode_problem(B, max_len=8192, seed=270 + B)
+        out = _run(p, max_seq_len=8192)
+        assert torch.isfinite(out.float()).all()
+        rng = np.random.default_rng(B)
+        pick = np.sort(rng.choice(B, size=min(B, 32), replace=False))
+        sub = {k: (v[pick] if k in ("q", "block_table", "seq_lens") else v) for k, v in p.items()}
+        _check(out[torch.from_numpy(pick).cuda()], oracle.decode_attention(**sub))
+
+
+def test_device_side_bad_inputs_reported_without_fault():
+    p = inputs.decode_problem(3, seq_lens=[10, 20, 30], seed=280)
+    d = _to_dev(p)
+    bi.get_device_error()
+    bad_lens = torch.tensor([10, 0, 30], dtype=torch.int32, device="cuda")
+    bi.decode_attention(d["q"], d["k_cache"], d["v_cache"], d["block_table"], bad_lens, max_seq_len=30)
+    with pytest.raises(bi.BiError, match="BAD_INPUT"):
+        bi.get_device_error()
+    bad_bt = d["block_table"].clone()
+    bad_bt[2, 0] = 10 ** 6
+    bi.decode_attention(d["q"], d["k_cache"], d["v_cache"], bad_bt, d["seq_lens"], max_seq_len=30)
+    with pytest.raises(bi.BiError, match="BAD_INPUT"):
+        bi.get_device_error()
+    # the context is still usable and later calls are clean
+    _check(_run(p), oracle.decode_attention(**p))
+    bi.get_device_error()
+
+
+def test_empty_batch_is_a_no_op():
+    p = inputs.decode_problem(1, seq_lens=[5], seed=290)
+    d = _to_dev(p)
+    out = bi.decode_attention(d["q"][:0], d["k_cache"], d["v_cache"], d["block_table"][:0],
+                              d["seq_lens"][:0], max_seq_len=5)
+    assert out.shape == (0, 32, 128)

@@ -1,0 +1,109 @@
+"""bi_rmsnorm on the GPU: parity with the fp64 oracle (<= 2 bf16 ulp) and
+bitwise batch invariance (row bits independent of batch size and position).
+
+Workload: hidden 4096, eps 1e-6, weight ~ N(1, 0.1), rows ~ N(0, 1) with 1% of
+elements scaled x100; batch sizes 1, 2, 3, 8, 64, 512, 2048, 16384.
+"""
+import numpy as np
+import pytest
+import torch
+
+import invariant_bi_rmsnorm_gb300 as bi
+import oracle
+from invariant_bi_rmsnorm_gb300 import inputs
+from tests._util import bits, ulp_distance
+
+pytestmark = pytest.mark.gpu
+
+H, EPS = 4096, 1e-6
+BATCHES = [1, 2, 3, 8, 64, 512, 2048, 16384]
+ULP_TOL = 2
+
+
+@pytest.fixture(scope="module")
+def pool():
+    x = inputs.rmsnorm_rows(max(BATCHES), H, seed=3)
+    w = inputs.rmsnorm_weight(H, seed=4)
+    ref = oracle.round_bf16(oracle.rmsnorm(x, w, EPS))
+    return x, w, x.cuda(), w.cuda(), ref
+
+
+def test_parity_full_pool_within_2_ulp(pool):
+    x, w, xd, wd, ref = pool
+    y = bits(bi.rmsnorm(xd, wd, EPS))
+    d = ulp_distance(y, ref)
+    assert d.max() <= ULP_TOL, f"max {d.max()} ulp at {np.unravel_index(d.argmax(), d.shape)}"
+
+
+def test_rows_bit_identical_across_batch_sizes(pool):
+    _, _, xd, wd, _ = pool
+    full = bits(bi.rmsnorm(xd, wd, EPS))
+    for B in BATCHES:
+        yb = bits(bi.rmsnorm(xd[:B].contiguous(), wd, EPS))
+        assert np.array_equal(yb, full[:B]), f"batch {B} differs from batch {max(BATCHES)}"
+
+
+def test_rows_bit_identical_under_permutation(pool):
+    _, _, xd, wd, _ = pool
+    B = 2048
+    full = bits(bi.rmsnorm(xd[:B].contiguous(), wd, EPS))
+    perm = torch.randperm(B, generator=torch.Generator().manual_seed(9))
+    yp = bits(bi.rmsnorm(xd[:B][perm.cuda()].contiguous(), wd, EPS))
+    assert np.array_equal(yp, full[perm.numpy()])
+
+
+def test_run_to_run_deterministic(pool):
+    _, _, xd, wd, _ = pool
+    a = bits(bi.rmsnorm(xd[:512].contiguous(), wd, EPS))
+    b = bits(bi.rmsnorm(xd[:512].contiguous(), wd, EPS))
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("hidden", [8, 128, 4104, 5120, 12288, 32768])
+def test_other_hidden_sizes(hidden):
+    # 8 and 128: one partial warp; 4104: a ragged warp; 12288: 3 vectors per
+    # thread (padded loop); 32768: the largest supported row
+    x = inputs.rmsnorm_rows(37, hidden, seed=hidden)
+    w = inputs.rmsnorm_weight(hidden, seed=hidden + 1)
+    y = bits(bi.rmsnorm(x.cuda(), w.cuda(), EPS))
+    ref = oracle.round_bf16(oracle.rmsnorm(x, w, EPS))
+    assert ulp_distance(y, ref).max() <= ULP_TOL
+    one = bits(bi.rmsnorm(x[20:21].cuda(), w.cuda(), EPS))
+    assert np.array_equal(one[0], y[20])
+
+
+def test_strided_rows_and_in_place():
+    x = inputs.rmsnorm_rows(10, 4096 + 64, seed=21)
+    w = inputs.rmsnorm_weight(4096, seed=22)
+    xd = x.cuda()
+    view = xd[:, :4096]  # leading dimension 4160
+    ref = oracle.round_bf16(oracle.rmsnorm(x[:, :4096].contiguous(), w, EPS))
+    y = bits(bi.rmsnorm(view, w.cuda(), EPS))
+    assert ulp_distance(y, ref).max() <= ULP_TOL
+    out = bi.rmsnorm(view, w.cuda(), EPS, out=view)  # in place
+    assert np.array_equal(bits(out), y)
+    assert np.array_equal(bits(xd[:, 4096:]), bits(x[:, 4096:]))  # padding untouched
+
+
+def test_special_rows():
+    # zero row, constant row, one-hot row, huge and tiny magnitudes (the sum
+    # of squares is kept in fp32, so rows stay well inside its range: the
+    # largest here sums to about 4e33)
+    Hs = 4096
+    rows = torch.zeros(5, Hs)
+    rows[1] = 3.0
+    rows[2, 17] = -250.0
+    rows[3] = 1.0e15
+    rows[4] = 1.0e-20
+    x = rows.to(torch.bfloat16)
+    w = inputs.rmsnorm_weight(Hs, seed=23)
+    y = bits(bi.rmsnorm(x.cuda(), w.cuda(), EPS))
+    ref = oracle.round_bf16(oracle.rmsnorm(x, w, EPS))
+    assert ulp_distance(y, ref).max() <= ULP_TOL
+
+
+def test_empty_batch_is_a_no_op():
+    w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
+    y = bi.rmsnorm(torch.empty(0, 4096, dtype=torch.bfloat16, device="cuda"), w, EPS)
+    assert y.shape == (0, 4096)
+    bi.get_device_error()
