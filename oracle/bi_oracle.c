@@ -132,7 +132,7 @@ int oracle_rmsnorm(const uint16_t* x, const uint16_t* w, int64_t rows,
 int oracle_gemm(const uint16_t* x, const uint16_t* W, int32_t M, int32_t N,
                 int32_t K, double* y) {
     if (M < 0 || N < 0 || K < 0) return -1;
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t m = 0; m < M; ++m) {
         for (int32_t n = 0; n < N; ++n) {
             double acc = 0.0;
