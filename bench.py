@@ -67,6 +67,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "attention", "rmsnorm"],
                     help="time one kernel of the path alone (for profiling); prints its own line")
+    ap.add_argument("--batch", type=int, default=ATT_B,
+                    help="sequences for --case attention (a smaller case for ncu captures)")
     return ap.parse_args()
 
 
@@ -547,13 +549,14 @@ def run_case(args):
         y = torch.empty(GEMM_M, N, dtype=torch.bfloat16, device=dev)
         fn, work, unit = (lambda: bi.gemm(x, W, out=y)), 2.0 * GEMM_M * N * K, "TFLOP/s"
     elif args.case == "attention":
-        p = inputs.decode_problem(ATT_B, max_len=MAX_LEN, seed=270, device=dev)
+        B = args.batch
+        p = inputs.decode_problem(B, max_len=MAX_LEN, seed=270, device=dev)
         a = {k: v.to(dev) for k, v in p.items()}
-        out = torch.empty(ATT_B, HQ, HD, dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(bi.decode_attention_workspace_size(ATT_B, HQ, HD, MAX_LEN),
+        out = torch.empty(B, HQ, HD, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bi.decode_attention_workspace_size(B, HQ, HD, MAX_LEN),
                          dtype=torch.uint8, device=dev)
         lens = p["seq_lens"].to(torch.int64)
-        work = float((lens * HKV * HD * 4).sum() + ATT_B * HQ * HD * 4 + 4 * ((lens + 15) // 16).sum())
+        work = float((lens * HKV * HD * 4).sum() + B * HQ * HD * 4 + 4 * ((lens + 15) // 16).sum())
         fn = lambda: bi.decode_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"],  # noqa: E731
                                          a["seq_lens"], max_seq_len=MAX_LEN, out=out, workspace=ws)
         unit = "GB/s"
