@@ -176,6 +176,45 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
                               int32_t max_seq_len, float scale, void* out, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * bi_decode_attention_noalloc -- bi_decode_attention for callers that cannot
+ * allocate device memory when they call it.
+ *
+ * Some callers have no way to obtain a workspace: a plugin handed only its
+ * input and output buffers by a host framework, a serving loop whose device
+ * memory was all reserved up front by a caching allocator (so a fresh
+ * cudaMalloc would fail, or would synchronise the device mid-step), or code
+ * that must not trigger allocation at all.  This entry point takes the same
+ * arguments minus the workspace and computes exactly what bi_decode_attention
+ * computes -- same kernels, same reduction order, bit-identical output --
+ * keeping the chunk partials in a scratch array that is part of the library's
+ * device image instead.  The pages this library follows describe no such
+ * entry point; it exists only for those callers.
+ *
+ * Limits and behaviour:
+ *   - the scratch holds 65536 chunk partials: B * Hq * ceil(max_seq_len/256)
+ *     must not exceed 65536 (for example 64 sequences of 32 heads up to 8192
+ *     tokens, or 256 sequences of 32 heads up to 2048 tokens); larger calls
+ *     return BI_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *   - the array takes 32.5 MiB of device memory on every GPU that loads the
+ *     library, for as long as the library stays loaded.
+ *   - nothing is allocated or freed: no cudaMalloc, no cudaFree, no library
+ *     allocator.  The first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture.
+ *   - every call on a device shares the one array and it keeps the last
+ *     call's partials; nothing in it needs to start at zero.  Calls whose
+ *     kernels may overlap on the GPU (different streams, without ordering
+ *     between them) race on it and must be serialised by the caller.
+ * Other arguments, errors and device-side checks: as bi_decode_attention.
+ */
+bi_status bi_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_table, int32_t max_pages_per_seq,
+                                      const int32_t* seq_lens, int32_t B, int32_t Hq,
+                                      int32_t Hkv, int32_t D, int32_t page_size,
+                                      int32_t num_pages, int32_t max_seq_len, float scale,
+                                      void* out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

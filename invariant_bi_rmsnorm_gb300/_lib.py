@@ -27,7 +27,7 @@ DECODE_CHUNK = 256
 EXPORTS = (
     "bi_abi_version", "bi_status_string", "bi_get_device_error", "bi_rmsnorm", "bi_gemm",
     "bi_decode_attention_workspace_size", "bi_decode_num_chunks", "bi_decode_chunk_len",
-    "bi_decode_attention",
+    "bi_decode_attention", "bi_decode_attention_noalloc",
 )
 
 _lib = None
@@ -67,5 +67,8 @@ def load() -> ctypes.CDLL:
                                         _i32, _i32, _i32, ctypes.c_float, _vp, _vp,
                                         ctypes.c_size_t, _vp]
     lib.bi_decode_attention.restype = ctypes.c_int
+    lib.bi_decode_attention_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                                _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp]
+    lib.bi_decode_attention_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib

@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
@@ -441,4 +442,60 @@ extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, con
         if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
     }
     return BI_OK;
+}
+
+// ---------------------------------------------------------------------------
+// bi_decode_attention_noalloc: the same computation for callers that cannot
+// allocate device memory at call time.  The chunk partials live in a fixed
+// array that is part of the library's own device image instead of a
+// caller-provided workspace.
+namespace {
+
+// Capacity in chunk partials (one per sequence x query head x 256-token
+// chunk), each kD + 2 floats: 65536 x 130 x 4 bytes = 32.5 MiB per device.
+constexpr int64_t kNoAllocPartials = 65536;
+constexpr size_t kNoAllocBytes = static_cast<size_t>(kNoAllocPartials) * (kD + 2) * sizeof(float);
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocPartials * (kD + 2)];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device.  The host-side
+// name of the array is only a stand-in; the address a kernel can use comes
+// from cudaGetSymbolAddress, resolved once per device with that device
+// current and cached.
+void* noalloc_scratch_address(int dev) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" bi_status bi_decode_attention_noalloc(const void* q, const void* k_cache,
+                                                 const void* v_cache, const int32_t* block_table,
+                                                 int32_t max_pages_per_seq,
+                                                 const int32_t* seq_lens, int32_t B, int32_t Hq,
+                                                 int32_t Hkv, int32_t D, int32_t page_size,
+                                                 int32_t num_pages, int32_t max_seq_len,
+                                                 float scale, void* out, cudaStream_t stream) {
+    if (B < 0 || Hq <= 0 || max_seq_len < 1) return BI_ERR_INVALID_ARG;
+    const int64_t partials = static_cast<int64_t>(B) * Hq * ceil_div(max_seq_len, kChunk);
+    const size_t need = bi_decode_attention_workspace_size(B, Hq, D, max_seq_len);
+    if (need > kNoAllocBytes || partials > kNoAllocPartials) return BI_ERR_WORKSPACE_TOO_SMALL;
+    void* ws = nullptr;
+    if (need > 0) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
+        ws = noalloc_scratch_address(dev);
+        if (!ws) return BI_ERR_CUDA;
+    }
+    return bi_decode_attention(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, B,
+                               Hq, Hkv, D, page_size, num_pages, max_seq_len, scale, out, ws,
+                               need > 0 ? kNoAllocBytes : 0, stream);
 }
