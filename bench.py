@@ -483,7 +483,7 @@ def cpu_baseline(wl):
     rows = 4
     probe = _oracle_sample({K: wl.gx[K][:rows].cpu() for K in wl.gx}, Ws, att,
                            wl.rx[:64].cpu(), wl.rw.cpu())
-    rows = int(max(4, min(256, rows * 12.0 / max(probe["gemm_s"], 1e-3))))
+    rows = int(max(4, min(2048, rows * 12.0 / max(probe["gemm_s"], 1e-3))))
     r = _oracle_sample({K: wl.gx[K][:rows].cpu() for K in wl.gx}, Ws, att,
                        wl.rx[:256].cpu(), wl.rw.cpu())
     return {"value": round(r["gemm_flops"] / r["gemm_s"] / 1e12, 6), "unit": "TFLOP/s",

@@ -93,7 +93,7 @@ bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int32_
  *
  * Operation: "2. Batch-Invariant Matrix Multiplication" of the same page: a
  * data-parallel tiled matmul with ONE kernel configuration for every shape --
- * a fixed 128x256 output tile, K walked in ascending 64-wide blocks, each
+ * a fixed 128x224 output tile, K walked in ascending 64-wide blocks, each
  * block as four ascending 16-deep tcgen05 MMAs accumulating in TMEM.  No
  * split-K or stream-K for any M, and the same MMA instruction shape always.
  *

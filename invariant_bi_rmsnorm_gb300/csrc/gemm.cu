@@ -6,15 +6,15 @@
 // data-parallel matmul gives each output tile to one core and reduces its
 // whole K range there; splitting K when M*N is small, or switching tensor-core
 // instruction or tile shape with the batch size, changes the reduction order.
-// So this kernel has exactly one tile shape (128 x 256), one MMA instruction
-// shape (tcgen05.mma kind::f16, M=128, N=256, K=16) and one K order (64-wide
+// So this kernel has exactly one tile shape (128 x 224), one MMA instruction
+// shape (tcgen05.mma kind::f16, M=128, N=224, K=16) and one K order (64-wide
 // blocks ascending, each as 4 ascending 16-deep MMAs into one fp32 TMEM
 // accumulator), whatever M, N and K are.  No split-K, no stream-K.
 //
 // Structure (persistent, one CTA per SM, warp-specialised):
-//   warp 0      TMA producer: x and W tiles (128x64 and 256x64 bf16, 128-byte
-//               swizzle) into a 4-stage shared-memory ring;
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//   warp 0      TMA producer: x and W tiles (128x64 and 224x64 bf16, 128-byte
+//               swizzle) into a 5-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns (two 128x224 fp32 accumulators) and
 //               issues the MMAs from one thread;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32*(w%4) ..), fp32 -> bf16 round-to-nearest-even, store.
@@ -28,14 +28,17 @@
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = 224;  // N = 224 keeps whole waves on 152 SMs for the usual layer widths
 constexpr int BK = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kABytes = BM * BK * 2;  // 16 KiB
-constexpr int kBBytes = BN * BK * 2;  // 32 KiB
+constexpr int kBBytes = BN * BK * 2;  // 28 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;  // 2 x 256 fp32 columns
+constexpr uint32_t kTmemCols = 512;  // two accumulators, at columns 0 and 256
+constexpr uint32_t kAccStride = 256;
+static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
+static_assert(BN % 16 == 0 && BN <= 256 && BN <= static_cast<int>(kAccStride), "tcgen05 M=128 shape");
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9
@@ -132,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 bi::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kAccStride;
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!bi::mbar_wait(&full[stage], phase)) {
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = mb * BM + quarter * 32 + lane;
             __nv_bfloat16* yrow = y + static_cast<int64_t>(row) * ld_y;
             const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc) * kAccStride;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 const int col0 = nb * BN + ch * 32;

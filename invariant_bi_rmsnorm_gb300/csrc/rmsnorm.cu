@@ -13,6 +13,7 @@
 //   2. each warp folds its 32 partials with an xor butterfly (16,8,4,2,1) and
 //      lane 0's result is taken;
 //   3. every thread folds the per-warp sums in warp order 0, 1, 2, ...
+// (hidden 4096: T = 256 threads, 2 vectors each.)
 // Then r = rsqrt(sum / hidden + eps) and y = bf16_rn((x * r) * w) in fp32.
 #include <cuda_bf16.h>
 
@@ -21,7 +22,10 @@
 
 namespace {
 
-constexpr int kMaxThreads = 512;
+// 256 threads per row: each thread keeps two 16-byte loads in flight at
+// hidden 4096, and 8 rows (CTAs) fit on an SM, which is what it takes to keep
+// HBM busy with one row per CTA (512 threads x 1 load left it latency-bound).
+constexpr int kMaxThreads = 256;
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -106,7 +110,7 @@ extern "C" bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t r
         vpt = 1;
     } else {
         threads = kMaxThreads;
-        vpt = (nvec + kMaxThreads - 1) / kMaxThreads;
+        vpt = (nvec + kMaxThreads - 1) / kMaxThreads;  // 2 .. 16
     }
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* wb = static_cast<const __nv_bfloat16*>(w);
@@ -118,7 +122,9 @@ extern "C" bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t r
         rmsnorm_kernel<2><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
     else if (vpt <= 4)
         rmsnorm_kernel<4><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
-    else
+    else if (vpt <= 8)
         rmsnorm_kernel<8><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+    else
+        rmsnorm_kernel<16><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
