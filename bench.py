@@ -265,6 +265,17 @@ class Workload:
         t = timeit(cublas)
         res["cublas_tflops"] = self.gemm_flops / (t * 1e-3) / 1e12
         res["cublas_ms"] = t
+        # fixed split COUNT attention (not batch-invariant), with the split
+        # count a split-KV kernel would pick to fill 152 SMs at this batch
+        ns = max(1, min(32, -(-2 * 152 // (ATT_B * HKV))))
+        a = self.att
+        ws_fc = torch.empty(self.bi.decode_attention_workspace_size(ATT_B, HQ, HD, ns * 256),
+                            dtype=torch.uint8, device=self.dev)
+        t = timeit(lambda: self.bi.decode_attention_fixed_splits(
+            a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"], MAX_LEN, ns,
+            out=self.att_out, workspace=ws_fc))
+        res["fixed_split_count_attention_gbs"] = self.att_bytes / (t * 1e-3) / 1e9
+        res["fixed_split_count"] = ns
         if hasattr(F, "rms_norm"):
             t = timeit(lambda: F.rms_norm(self.rx, (HIDDEN,), self.rw, EPS))
             res["torch_rms_norm_gbs"] = self.rms_bytes / (t * 1e-3) / 1e9
@@ -368,6 +379,9 @@ def run_ours(args):
                 "frac_of_measured_hbm": round(att_gbs / world / hbm, 4),
                 "frac_of_8tbs": round(att_gbs / world / NOMINAL_HBM_GBS, 4),
                 "algorithmic_bytes_per_step": wl.att_bytes,
+                "fixed_split_count_gbs_same_run": round(refs["fixed_split_count_attention_gbs"], 1),
+                "fixed_split_count": refs["fixed_split_count"],
+                "cost_vs_fixed_split_count": round(refs["fixed_split_count_attention_gbs"] / (att_gbs / world), 4),
                 "traffic": traffic_record("bi_decode_attention")},
             "bi_rmsnorm": {
                 "gbs": round(rms_gbs / world, 1), "ms_per_step": round(rms_ms / K, 4),

@@ -65,6 +65,15 @@ const char* bi_status_string(bi_status s);
  * Returns BI_OK, BI_ERR_DEVICE_TIMEOUT, BI_ERR_DEVICE_BAD_INPUT or BI_ERR_CUDA. */
 bi_status bi_get_device_error(cudaStream_t stream);
 
+/* Self-test of the device-side timeout path: launch one CTA whose bounded
+ * barrier wait is made to run out -- it waits for `limit_us` microseconds
+ * (1 .. 2,000,000) on an mbarrier nothing arrives on, then records
+ * BI_ERR_DEVICE_TIMEOUT in the error word and exits normally.  The wait
+ * routine is the one every kernel of the library uses (their limit is about
+ * two seconds).  Read the result with bi_get_device_error.  Errors:
+ * INVALID_ARG, CUDA. */
+bi_status bi_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream);
+
 /*
  * bi_rmsnorm -- y[r][i] = bf16( x[r][i] * rsqrt(mean_j x[r][j]^2 + eps) * w[i] )
  *
@@ -175,6 +184,30 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
                               int32_t D, int32_t page_size, int32_t num_pages,
                               int32_t max_seq_len, float scale, void* out, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bi_decode_attention_fixed_splits -- the same attention with a fixed split
+ * COUNT instead of a fixed split size: each sequence's pages are cut into
+ * num_splits nearly equal runs (ceil(ceil(L/16)/num_splits) pages each), so
+ * the chunk size -- and the reduction order -- changes as the sequence grows.
+ * This is the strategy "Defeating Nondeterminism in LLM Inference: The Core
+ * Role of Batch Invariance" warns against (section "3. Batch-Invariant
+ * Attention", figure "Fixed Number Split KV Strategy"); it is NOT batch- or
+ * growth-invariant and exists only as the non-invariant comparison: a
+ * negative control for the growth tests and a same-run cost reference.
+ *   num_splits   1 .. ; ceil(ceil(max_seq_len/16)/num_splits) <= 512 pages.
+ *   workspace    >= bi_decode_attention_workspace_size(B, Hq, D,
+ *                num_splits * 256) bytes when num_splits >= 2.
+ * Other arguments and errors: as bi_decode_attention.
+ */
+bi_status bi_decode_attention_fixed_splits(const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_table,
+                                           int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                           int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                           int32_t page_size, int32_t num_pages,
+                                           int32_t max_seq_len, float scale, int32_t num_splits,
+                                           void* out, void* workspace, size_t workspace_bytes,
+                                           cudaStream_t stream);
 
 /*
  * bi_decode_attention_noalloc -- bi_decode_attention for callers that cannot

@@ -23,7 +23,8 @@ import torch
 from . import _lib
 from ._lib import DECODE_CHUNK, PAGE_SIZE
 
-__all__ = ["BiError", "rmsnorm", "gemm", "decode_attention", "decode_attention_workspace_size",
+__all__ = ["BiError", "rmsnorm", "gemm", "decode_attention", "decode_attention_fixed_splits",
+           "decode_attention_workspace_size", "selftest_wait_timeout",
            "decode_num_chunks", "decode_chunk_len", "get_device_error", "abi_version",
            "status_string", "PAGE_SIZE", "DECODE_CHUNK"]
 
@@ -133,6 +134,53 @@ def decode_num_chunks(seq_len: int) -> int:
 
 def decode_chunk_len(seq_len: int, c: int) -> int:
     return int(_lib.load().bi_decode_chunk_len(seq_len, c))
+
+
+def selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the device timeout self-test (a bounded wait that must run out);
+    read its outcome with get_device_error()."""
+    _check(_lib.load().bi_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "bi_selftest_wait_timeout")
+
+
+def _attention_args(q, k_cache, v_cache, block_table, seq_lens):
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _cuda_bf16(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens")):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("decode_attention: q [B,Hq,D] and caches [P,Hkv,page,D] expected")
+    B, Hq, D = q.shape
+    num_pages, Hkv, page, D2 = k_cache.shape
+    if D2 != D or block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("decode_attention: inconsistent shapes")
+    return B, Hq, D, num_pages, Hkv, page
+
+
+def decode_attention_fixed_splits(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
+                                  num_splits: int, scale: float | None = None, out=None,
+                                  workspace=None, stream=None) -> torch.Tensor:
+    """Fixed split-COUNT attention: NOT batch- or growth-invariant.  The
+    comparison variant (negative control and cost reference) only."""
+    B, Hq, D, num_pages, Hkv, page = _attention_args(q, k_cache, v_cache, block_table, seq_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    need = decode_attention_workspace_size(B, Hq, D, int(num_splits) * DECODE_CHUNK)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.load().bi_decode_attention_fixed_splits(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+        block_table.shape[1], seq_lens.data_ptr(), B, Hq, Hkv, D, page, num_pages,
+        int(max_seq_len), float(scale), int(num_splits), out.data_ptr(), ws_ptr, ws_bytes,
+        _stream(stream)), "bi_decode_attention_fixed_splits")
+    return out
 
 
 def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

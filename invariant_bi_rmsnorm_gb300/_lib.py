@@ -27,7 +27,8 @@ DECODE_CHUNK = 256
 EXPORTS = (
     "bi_abi_version", "bi_status_string", "bi_get_device_error", "bi_rmsnorm", "bi_gemm",
     "bi_decode_attention_workspace_size", "bi_decode_num_chunks", "bi_decode_chunk_len",
-    "bi_decode_attention", "bi_decode_attention_noalloc",
+    "bi_decode_attention", "bi_decode_attention_noalloc", "bi_decode_attention_fixed_splits",
+    "bi_selftest_wait_timeout",
 )
 
 _lib = None
@@ -70,5 +71,11 @@ def load() -> ctypes.CDLL:
     lib.bi_decode_attention_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
                                                 _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp]
     lib.bi_decode_attention_noalloc.restype = ctypes.c_int
+    lib.bi_decode_attention_fixed_splits.argtypes = [
+        _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
+        _i32, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.bi_decode_attention_fixed_splits.restype = ctypes.c_int
+    lib.bi_selftest_wait_timeout.argtypes = [_i32, _vp]
+    lib.bi_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
     return lib

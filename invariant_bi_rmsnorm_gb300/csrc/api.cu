@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "bi_internal.h"
+#include "bi_ptx.cuh"
 
 namespace {
 
@@ -25,6 +26,20 @@ int current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+// One thread waits, through the same bounded wait every kernel uses, on an
+// mbarrier that nothing will ever arrive on; the wait must give up after
+// `limit_ns` and record BI_ERR_DEVICE_TIMEOUT.
+__global__ void selftest_wait_kernel(uint32_t* err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        bi::mbar_init(&bar, 1);
+        bi::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !bi::mbar_wait_for(&bar, 0, limit_ns))
+        bi::report_error(err, bi::kErrTimeout | bi::kWhereSelftest);
 }
 
 }  // namespace
@@ -99,6 +114,14 @@ const char* bi_status_string(bi_status s) {
         case BI_ERR_DEVICE_BAD_INPUT: return "BI_ERR_DEVICE_BAD_INPUT";
     }
     return "BI_ERR_UNKNOWN";
+}
+
+bi_status bi_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream) {
+    if (limit_us < 1 || limit_us > 2000000) return BI_ERR_INVALID_ARG;
+    uint32_t* err = bi::device_error_word();
+    if (!err) return BI_ERR_CUDA;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(err, static_cast<uint64_t>(limit_us) * 1000u);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
 bi_status bi_get_device_error(cudaStream_t stream) {

@@ -62,14 +62,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // false) once about kWaitNs nanoseconds have passed since the first check of
 // the clock, or after kWaitPollLimit polls, whichever comes first, so a
 // barrier that never completes cannot hold the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1; i < kWaitPollLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitNs) return false;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitNs);
 }
 
 // ------------------------------------------------------------------ TMA ----

@@ -49,7 +49,9 @@ constexpr int kHalfBytes = kPage * 64 * 2;         // 16 rows x 64 dims: one TMA
 constexpr int kMatBytes = 2 * kHalfBytes;          // one (page, kv-head) K or V block
 constexpr int kStageBytes = 2 * kMatBytes;         // K + V
 constexpr int kMaxGroup = 8;                       // query heads per kv-head (mma N)
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*bars, pages*/;
+constexpr int kMaxPagesPerCta = 512;                // page list of one chunk (fixed-count variant)
+constexpr int kSmemBytes =
+    kStages * kStageBytes + 1024 /*align*/ + 64 /*bars*/ + 4 * kMaxPagesPerCta /*pages*/;
 
 static_assert(kStages * kStageBytes >= kWarps * (2 * kMaxGroup + kMaxGroup * kD) * 4,
               "combine area must fit in the stage ring");
@@ -75,8 +77,21 @@ struct SplitArgs {
     int num_pages;
     int max_seq_len;
     int max_chunks;
+    int num_splits;    // 0: fixed 256-token chunks; > 0: fixed split count (comparison variant)
     float scale_log2;  // scale * log2(e)
 };
+
+// Chunk geometry of one sequence of L tokens: pages per chunk and chunk count.
+// Fixed split size (num_splits == 0, the batch-invariant method): 16 pages =
+// 256 tokens per chunk, whatever L is.  Fixed split count (num_splits > 0),
+// the strategy the pages warn against and kept here only as a comparison: the
+// sequence's pages are cut into num_splits nearly equal runs, so the chunk
+// size, and with it the reduction order, changes as L grows.
+__device__ __forceinline__ void chunk_geometry(int L, int num_splits, int& ppc, int& nch) {
+    const int npg = (L + kPage - 1) / kPage;
+    ppc = num_splits > 0 ? (npg + num_splits - 1) / num_splits : kPagesPerChunk;
+    nch = (npg + ppc - 1) / ppc;
+}
 
 __global__ void __launch_bounds__(kThreads)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -93,10 +108,11 @@ __global__ void __launch_bounds__(kThreads)
         if (tid == 0 && c == 0 && g == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
         return;
     }
-    const int nch = (L + kChunk - 1) / kChunk;
+    int ppc, nch;
+    chunk_geometry(L, a.num_splits, ppc, nch);
     if (c >= nch) return;
-    const int t0 = c * kChunk;
-    const int ntok = min(kChunk, L - t0);
+    const int t0 = c * ppc * kPage;
+    const int ntok = min(ppc * kPage, L - t0);
     const int npages = (ntok + kPage - 1) / kPage;
 
     extern __shared__ uint8_t smem_raw[];
@@ -114,12 +130,12 @@ __global__ void __launch_bounds__(kThreads)
         bi::tma_prefetch_desc(&tmap_v);
     }
     __syncthreads();
-    if (tid < npages) {
-        const int pg = a.block_table[static_cast<int64_t>(s) * a.max_pages_per_seq + c * kPagesPerChunk + tid];
+    for (int i = tid; i < npages; i += kThreads) {
+        const int pg = a.block_table[static_cast<int64_t>(s) * a.max_pages_per_seq + c * ppc + i];
         if (pg < 0 || pg >= a.num_pages) {
             bad_page = 1;
         } else {
-            rows_s[tid] = (pg * a.Hkv + g) * kPage;
+            rows_s[i] = (pg * a.Hkv + g) * kPage;
         }
     }
     __syncthreads();
@@ -320,13 +336,14 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kD)
     attn_merge_kernel(const int32_t* __restrict__ seq_lens, const float* __restrict__ ws_acc,
                       const float* __restrict__ ws_ml, __nv_bfloat16* __restrict__ out, int Hq,
-                      int max_chunks, int max_seq_len) {
+                      int max_chunks, int max_seq_len, int num_splits) {
     const int hq = blockIdx.x;
     const int s = blockIdx.y;
     const int d = threadIdx.x;
     const int L = seq_lens[s];
     if (L < 1 || L > max_seq_len) return;  // reported by the split kernel
-    const int nch = (L + kChunk - 1) / kChunk;
+    int ppc, nch;
+    chunk_geometry(L, num_splits, ppc, nch);
     if (nch < 2) return;
     const int64_t base = (static_cast<int64_t>(s) * Hq + hq) * max_chunks;
     float M = ws_ml[base * 2];
@@ -369,15 +386,19 @@ extern "C" int32_t bi_decode_chunk_len(int32_t seq_len, int32_t c) {
     return c < n - 1 ? kChunk : seq_len - (n - 1) * kChunk;
 }
 
-extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache,
-                                         const int32_t* block_table, int32_t max_pages_per_seq,
-                                         const int32_t* seq_lens, int32_t B, int32_t Hq,
-                                         int32_t Hkv, int32_t D, int32_t page_size,
-                                         int32_t num_pages, int32_t max_seq_len, float scale,
-                                         void* out, void* workspace, size_t workspace_bytes,
-                                         cudaStream_t stream) {
+namespace {
+
+// Validate and launch split + merge.  num_splits == 0 is the batch-invariant
+// fixed split size; num_splits > 0 the fixed-split-count comparison variant,
+// whose workspace then holds num_splits partials per (sequence, query head).
+bi_status launch_attention(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, int32_t max_pages_per_seq,
+                           const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                           int32_t page_size, int32_t num_pages, int32_t max_seq_len, float scale,
+                           void* out, void* workspace, size_t workspace_bytes, int32_t num_splits,
+                           cudaStream_t stream) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || max_pages_per_seq < 1 || num_pages < 1 ||
-        max_seq_len < 1)
+        max_seq_len < 1 || num_splits < 0)
         return BI_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return BI_ERR_INVALID_ARG;
     if (D != kD || page_size != kPage) return BI_ERR_UNSUPPORTED_SHAPE;
@@ -387,14 +408,18 @@ extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, con
         return BI_ERR_UNSUPPORTED_SHAPE;
     if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages_per_seq) * kPage)
         return BI_ERR_INVALID_ARG;
+    if (num_splits > 0 && ceil_div(ceil_div(max_seq_len, kPage), num_splits) > kMaxPagesPerCta)
+        return BI_ERR_UNSUPPORTED_SHAPE;
     if (B == 0) return BI_OK;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return BI_ERR_INVALID_ARG;
     if (!bi::aligned16(q) || !bi::aligned16(k_cache) || !bi::aligned16(v_cache) ||
         !bi::aligned16(out) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
         (reinterpret_cast<uintptr_t>(seq_lens) & 3))
         return BI_ERR_MISALIGNED;
-    const int max_chunks = ceil_div(max_seq_len, kChunk);
-    const size_t need = bi_decode_attention_workspace_size(B, Hq, D, max_seq_len);
+    const int max_chunks = num_splits > 0 ? num_splits : ceil_div(max_seq_len, kChunk);
+    const size_t need = max_chunks >= 2 ? static_cast<size_t>(B) * Hq * max_chunks *
+                                              (static_cast<size_t>(D) + 2) * sizeof(float)
+                                        : 0;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return BI_ERR_WORKSPACE_TOO_SMALL;
         if (!bi::aligned16(workspace)) return BI_ERR_MISALIGNED;
@@ -432,16 +457,43 @@ extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, con
     args.num_pages = num_pages;
     args.max_seq_len = max_seq_len;
     args.max_chunks = max_chunks;
+    args.num_splits = num_splits;
     args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
     attn_split_kernel<<<dim3(max_chunks, Hkv, B), kThreads, kSmemBytes, stream>>>(tk, tv, args);
     if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
     if (max_chunks >= 2) {
         attn_merge_kernel<<<dim3(Hq, B), kD, 0, stream>>>(seq_lens, args.ws_acc, args.ws_ml,
-                                                          args.out, Hq, max_chunks, max_seq_len);
+                                                          args.out, Hq, max_chunks, max_seq_len,
+                                                          num_splits);
         if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
     }
     return BI_OK;
+}
+
+}  // namespace
+
+extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, int32_t max_pages_per_seq,
+                                         const int32_t* seq_lens, int32_t B, int32_t Hq,
+                                         int32_t Hkv, int32_t D, int32_t page_size,
+                                         int32_t num_pages, int32_t max_seq_len, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+    return launch_attention(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, B, Hq,
+                            Hkv, D, page_size, num_pages, max_seq_len, scale, out, workspace,
+                            workspace_bytes, 0, stream);
+}
+
+extern "C" bi_status bi_decode_attention_fixed_splits(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+    int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv,
+    int32_t D, int32_t page_size, int32_t num_pages, int32_t max_seq_len, float scale,
+    int32_t num_splits, void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (num_splits < 1) return BI_ERR_INVALID_ARG;
+    return launch_attention(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, B, Hq,
+                            Hkv, D, page_size, num_pages, max_seq_len, scale, out, workspace,
+                            workspace_bytes, num_splits, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -135,6 +135,17 @@ def test_decode_attention_argument_validation(lib):
     assert call(B=0) == _lib.BI_OK
 
 
+def test_selftest_and_fixed_splits_validation(lib):
+    assert lib.bi_selftest_wait_timeout(0, None) == _lib.BI_ERR_INVALID_ARG
+    assert lib.bi_selftest_wait_timeout(2000001, None) == _lib.BI_ERR_INVALID_ARG
+    f = lib.bi_decode_attention_fixed_splits
+    args = [FAKE, FAKE, FAKE, FAKE, 64, FAKE, 4, 32, 8, 128, 16, 256, 1000, 0.088]
+    assert f(*args, 0, FAKE, FAKE, 10 ** 9, None) == _lib.BI_ERR_INVALID_ARG      # no splits
+    assert f(*args, 4, FAKE, FAKE, 100, None) == _lib.BI_ERR_WORKSPACE_TOO_SMALL
+    big = [FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 4, 32, 8, 128, 16, 256, 16384, 0.088]
+    assert f(*big, 1, FAKE, FAKE, 10 ** 9, None) == _lib.BI_ERR_UNSUPPORTED_SHAPE  # 1024 pages per split
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     import invariant_bi_rmsnorm_gb300 as bi

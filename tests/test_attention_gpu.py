@@ -256,3 +256,48 @@ def test_empty_batch_is_a_no_op():
     out = bi.decode_attention(d["q"][:0], d["k_cache"], d["v_cache"], d["block_table"][:0],
                               d["seq_lens"][:0], max_seq_len=5)
     assert out.shape == (0, 32, 128)
+
+
+# ------------------------------------- fixed split COUNT: negative control ---
+def _flashdecoding_splits(B, Hkv=8, sms=152):
+    """A split count chosen to fill the GPU, as split-KV kernels commonly do:
+    more splits when fewer sequences are in flight."""
+    return max(1, min(32, -(-2 * sms // (B * Hkv))))
+
+
+def test_fixed_split_count_matches_oracle():
+    p = inputs.decode_problem(5, seq_lens=[1, 100, 1000, 3000, 8192], seed=310)
+    d = _to_dev(p)
+    ref = oracle.decode_attention(**p)
+    for ns in (1, 3, 16):
+        out = bi.decode_attention_fixed_splits(d["q"], d["k_cache"], d["v_cache"],
+                                               d["block_table"], d["seq_lens"], max_seq_len=8192,
+                                               num_splits=ns)
+        _check(out, ref)
+
+
+def test_fixed_split_count_breaks_invariance_where_fixed_size_does_not():
+    # The same sequences run alone (B = 1) and in a batch of 128: with the
+    # split count following the batch size the bits change; with the fixed
+    # 256-token split size they never do.  The first half is the negative
+    # control that shows the invariance checks can fail.
+    B = 128
+    p = inputs.decode_problem(B, max_len=8192, seed=320)
+    d = _to_dev(p)
+    ns_batch, ns_alone = _flashdecoding_splits(B), _flashdecoding_splits(1)
+    assert ns_batch != ns_alone
+    batched_fc = bits(bi.decode_attention_fixed_splits(
+        d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], 8192, ns_batch))
+    batched_fs = bits(bi.decode_attention(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                          d["seq_lens"], 8192))
+    changed = 0
+    for s in range(0, B, 8):
+        sl = slice(s, s + 1)
+        alone_fc = bits(bi.decode_attention_fixed_splits(
+            d["q"][sl], d["k_cache"], d["v_cache"], d["block_table"][sl], d["seq_lens"][sl],
+            8192, ns_alone))
+        alone_fs = bits(bi.decode_attention(d["q"][sl], d["k_cache"], d["v_cache"],
+                                            d["block_table"][sl], d["seq_lens"][sl], 8192))
+        changed += int(not np.array_equal(alone_fc[0], batched_fc[s]))
+        assert np.array_equal(alone_fs[0], batched_fs[s])
+    assert changed > 0, "the fixed-count control never changed: the comparison would have no teeth"
