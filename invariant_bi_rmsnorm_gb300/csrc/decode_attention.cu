@@ -8,27 +8,34 @@
 // the KV sequence is split -- but by a fixed split SIZE, so the reduction
 // order of a sequence depends only on its own length.
 //
-// Kernel 1 (split): one CTA per (sequence s, kv-head g, chunk c).  The chunk
-// is tokens [256c, min(256c + 256, L)), i.e. up to 16 pages of 16 tokens.
-// Warp w (of 4) owns the chunk's pages w, w+4, w+8, w+12 and runs an online
-// softmax over them in that order, for the Hq/Hkv query heads that share
-// kv-head g.  Pages arrive by TMA (2-D tiled loads, 128-byte swizzle) into a
-// 2-stage ring per warp.  Per page:
+// Kernel 1 (split): one CTA per (sequence s, kv-head g, group of consecutive
+// chunks).  Chunk c is tokens [256c, min(256c + 256, L)), i.e. up to 16 pages
+// of 16 tokens.  For each chunk, warp w (of 4) owns the chunk's pages w, w+4,
+// w+8, w+12 and runs an online softmax over them in that order, for the
+// Hq/Hkv query heads that share kv-head g.  Pages arrive by TMA (2-D tiled
+// loads, 128-byte swizzle) into a 2-stage ring per warp that runs on across
+// chunk boundaries.  Per page:
 //     S^T[16 tok x 8 heads] = K_page[16 x 128] . Q^T[128 x 8]   (8 mma.sync)
 //     p = exp2(S * scale * log2 e - m_new), rounded to bf16
 //     O^T[128 x 8] = O^T * alpha + V^T[128 x 16] . P^T[16 x 8]   (8 mma.sync)
-// The four warp states are then folded in warp order 0..3.  A sequence with
-// one chunk is normalised and written here; otherwise the chunk partial
-// (m, l, O) goes to the workspace.
-// Kernel 2 (merge): for each (sequence, query head) with more than one chunk,
-// fold the partials in ascending chunk order with the log-sum-exp rule and
-// write bf16(O / l).
+// At the end of each chunk the four warp states are folded in warp order
+// 0..3 into the chunk partial (m, l, O).  If the CTA's group holds every
+// chunk of the sequence, it folds the partials in ascending chunk order with
+// the log-sum-exp rule and writes bf16(O / l); otherwise the partials go to
+// the workspace.
+// Kernel 2 (merge): for each (sequence, query head) not finished by one CTA,
+// fold the partials in ascending chunk order -- the same fp32 operations in
+// the same order -- and write bf16(O / l).
+// How many chunks a CTA walks is chosen per launch to fill the GPU; it moves
+// work between CTAs but never changes any operation or its order, so it
+// cannot change a bit of the result.
 //
 // Tokens past the sequence end inside its last page are masked to -inf and
 // their V rows are zeroed in shared memory before use, so whatever the cache
 // holds there (a later token, or uninitialised bits) never reaches the result.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -49,12 +56,11 @@ constexpr int kHalfBytes = kPage * 64 * 2;         // 16 rows x 64 dims: one TMA
 constexpr int kMatBytes = 2 * kHalfBytes;          // one (page, kv-head) K or V block
 constexpr int kStageBytes = 2 * kMatBytes;         // K + V
 constexpr int kMaxGroup = 8;                       // query heads per kv-head (mma N)
-constexpr int kMaxPagesPerCta = 512;                // page list of one chunk (fixed-count variant)
-constexpr int kSmemBytes =
-    kStages * kStageBytes + 1024 /*align*/ + 64 /*bars*/ + 4 * kMaxPagesPerCta /*pages*/;
-
-static_assert(kStages * kStageBytes >= kWarps * (2 * kMaxGroup + kMaxGroup * kD) * 4,
-              "combine area must fit in the stage ring");
+constexpr int kMaxPagesPerCta = 512;                // pages one CTA walks (a chunk group)
+constexpr int kMaxChunksPerCta = kMaxPagesPerCta / kPagesPerChunk;  // 32
+constexpr int kFoldFloats = kMaxGroup * kD + kWarps * 2 * kMaxGroup;  // chunk-fold buffers
+constexpr int kSmemBytes = kStages * kStageBytes + kFoldFloats * 4 + 4 * kMaxPagesPerCta +
+                           8 * kStages + 1024 /*align*/;  // 71.2 KB: 3 CTAs per SM
 
 // Byte offset of the 16-byte chunk `ch` (0..15) of row `r` (0..15) inside one
 // K or V page block as laid down by two 16x64 TMA boxes with 128-byte
@@ -78,6 +84,7 @@ struct SplitArgs {
     int max_seq_len;
     int max_chunks;
     int num_splits;    // 0: fixed 256-token chunks; > 0: fixed split count (comparison variant)
+    int chunks_per_cta;  // consecutive chunks one CTA walks (a schedule choice only)
     float scale_log2;  // scale * log2(e)
 };
 
@@ -96,7 +103,7 @@ __device__ __forceinline__ void chunk_geometry(int L, int num_splits, int& ppc, 
 __global__ void __launch_bounds__(kThreads)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
-    const int c = blockIdx.x;
+    const int cg = blockIdx.x;  // chunk group
     const int g = blockIdx.y;
     const int s = blockIdx.z;
     const int tid = threadIdx.x;
@@ -105,21 +112,26 @@ __global__ void __launch_bounds__(kThreads)
 
     const int L = a.seq_lens[s];
     if (L < 1 || L > a.max_seq_len) {
-        if (tid == 0 && c == 0 && g == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+        if (tid == 0 && cg == 0 && g == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
         return;
     }
     int ppc, nch;
     chunk_geometry(L, a.num_splits, ppc, nch);
-    if (c >= nch) return;
-    const int t0 = c * ppc * kPage;
-    const int ntok = min(ppc * kPage, L - t0);
-    const int npages = (ntok + kPage - 1) / kPage;
+    const int c0 = cg * a.chunks_per_cta;
+    if (c0 >= nch) return;
+    const int c1 = min(nch, c0 + a.chunks_per_cta);
+    const bool whole = (c0 == 0 && c1 == nch);  // this CTA folds the whole sequence
+    const int npg_total = (L + kPage - 1) / kPage;
+    const int pg0 = c0 * ppc;
+    const int npg_group = min(c1 * ppc, npg_total) - pg0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    int32_t* rows_s = reinterpret_cast<int32_t*>(bars + kStages);  // TMA row of each page
+    float* fold_o = reinterpret_cast<float*>(smem + kStages * kStageBytes);  // [8 heads][128]
+    float* fold_ml = fold_o + kMaxGroup * kD;                                // [4 warps][m 8, l 8]
+    int32_t* rows_s = reinterpret_cast<int32_t*>(fold_ml + kWarps * 2 * kMaxGroup);  // TMA row per page
+    uint64_t* bars = reinterpret_cast<uint64_t*>(rows_s + kMaxPagesPerCta);
     __shared__ int bad_page;
 
     if (tid == 0) {
@@ -130,8 +142,8 @@ __global__ void __launch_bounds__(kThreads)
         bi::tma_prefetch_desc(&tmap_v);
     }
     __syncthreads();
-    for (int i = tid; i < npages; i += kThreads) {
-        const int pg = a.block_table[static_cast<int64_t>(s) * a.max_pages_per_seq + c * ppc + i];
+    for (int i = tid; i < npg_group; i += kThreads) {
+        const int pg = a.block_table[static_cast<int64_t>(s) * a.max_pages_per_seq + pg0 + i];
         if (pg < 0 || pg >= a.num_pages) {
             bad_page = 1;
         } else {
@@ -144,24 +156,34 @@ __global__ void __launch_bounds__(kThreads)
         return;
     }
 
+    auto pages_in = [&](int c) { return min(ppc, npg_total - c * ppc); };
     auto stage_ptr = [&](int st) { return smem + st * kStageBytes; };
-    auto issue = [&](int j) {  // warp-local page j -> stage warp*2 + (j & 1)
-        const int p = warp + kWarps * j;
-        const int st = warp * kStagesPerWarp + (j & 1);
-        uint8_t* kd = stage_ptr(st);
-        uint8_t* vd = kd + kMatBytes;
-        const int row = rows_s[p];
-        bi::mbar_arrive_expect_tx(&bars[st], kStageBytes);
-        bi::tma_load_2d(kd, &tmap_k, &bars[st], 0, row);
-        bi::tma_load_2d(kd + kHalfBytes, &tmap_k, &bars[st], 64, row);
-        bi::tma_load_2d(vd, &tmap_v, &bars[st], 0, row);
-        bi::tma_load_2d(vd + kHalfBytes, &tmap_v, &bars[st], 64, row);
-    };
 
-    const int my_pages = (npages > warp) ? (npages - warp + kWarps - 1) / kWarps : 0;
-    if (lane == 0) {
-        for (int j = 0; j < my_pages && j < kStagesPerWarp; ++j) issue(j);
-    }
+    // This warp's pages, in order: for each chunk of the group, pages warp,
+    // warp + 4, warp + 8, ... of that chunk.  The loader runs two pages ahead
+    // of the compute loop through a 2-stage ring; every lane tracks the
+    // loader position, lane 0 issues the copies.
+    int lc = c0, lp = warp, lj = 0;
+    while (lc < c1 && lp >= pages_in(lc)) { ++lc; lp = warp; }
+    auto issue_next = [&]() {
+        if (lc >= c1) return;
+        if (lane == 0) {
+            const int st = warp * kStagesPerWarp + (lj & 1);
+            uint8_t* kd = stage_ptr(st);
+            uint8_t* vd = kd + kMatBytes;
+            const int row = rows_s[(lc - c0) * ppc + lp];
+            bi::mbar_arrive_expect_tx(&bars[st], kStageBytes);
+            bi::tma_load_2d(kd, &tmap_k, &bars[st], 0, row);
+            bi::tma_load_2d(kd + kHalfBytes, &tmap_k, &bars[st], 64, row);
+            bi::tma_load_2d(vd, &tmap_v, &bars[st], 0, row);
+            bi::tma_load_2d(vd + kHalfBytes, &tmap_v, &bars[st], 64, row);
+        }
+        ++lj;
+        lp += kWarps;
+        while (lc < c1 && lp >= pages_in(lc)) { ++lc; lp = warp; }
+    };
+    issue_next();
+    issue_next();
 
     // Q^T as the mma B operand: lane holds head (lane/4) of the group and
     // dims 16ks + 2(lane%4) + {0,1} (b0) and +8 (b1).
@@ -178,154 +200,191 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
 
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
-    float acc[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-
     // ldmatrix lane roles
-    const int lm_j = lane >> 3;        // which 8x8 matrix this lane addresses
-    const int lm_r = lane & 7;         // row within it
-    int timed_out_at = -1;
-
-    for (int j = 0; j < my_pages; ++j) {
-        const int p = warp + kWarps * j;
-        const int st = warp * kStagesPerWarp + (j & 1);
-        if (!bi::mbar_wait(&bars[st], (j >> 1) & 1)) {
-            timed_out_at = j;
-            break;
-        }
-        const uint32_t ks_base = bi::smem_u32(stage_ptr(st));
-        const uint32_t vs_base = ks_base + kMatBytes;
-        const int valid = min(kPage, ntok - p * kPage);
-        if (valid < kPage) {
-            // zero V rows past the sequence end (16-byte units)
-            uint8_t* vd = stage_ptr(st) + kMatBytes;
-            for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
-                const int r = valid + (idx >> 4), ch = idx & 15;
-                *reinterpret_cast<uint4*>(vd + swz(r, ch)) = make_uint4(0, 0, 0, 0);
-            }
-            __syncwarp();
-        }
-
-        // S^T = K . Q^T  (tokens on M, heads on N), dims in ascending 16-blocks
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            const int r = lm_r + 8 * (lm_j & 1);
-            const int ch = 2 * ks + (lm_j >> 1);
-            bi::ldmatrix_x4(ks_base + swz(r, ch), a0, a1, a2, a3);
-            bi::mma_bf16_16816(sc, a0, a1, a2, a3, qb0[ks], qb1[ks]);
-        }
-        // sc[0], sc[1]: token lane/4, heads 2(lane%4)+{0,1}; sc[2], sc[3]: token +8
-        const int tokA = lane >> 2, tokB = tokA + 8;
-        const float x0 = tokA < valid ? sc[0] * a.scale_log2 : -INFINITY;
-        const float x1 = tokA < valid ? sc[1] * a.scale_log2 : -INFINITY;
-        const float x2 = tokB < valid ? sc[2] * a.scale_log2 : -INFINITY;
-        const float x3 = tokB < valid ? sc[3] * a.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-        const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
-        const uint32_t pA = bi::pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
-        const uint32_t pB = bi::pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
-        // the row sums use the same bf16-rounded weights that multiply V
-        float ps0 = __uint_as_float(pA << 16) + __uint_as_float(pB << 16);
-        float ps1 = __uint_as_float(pA & 0xffff0000u) + __uint_as_float(pB & 0xffff0000u);
-#pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) {
-            ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
-            ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
-        }
-        l_run[0] = __fmaf_rn(l_run[0], al0, ps0);
-        l_run[1] = __fmaf_rn(l_run[1], al1, ps1);
-        m_run[0] = mn0;
-        m_run[1] = mn1;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            acc[mt][0] *= al0;
-            acc[mt][1] *= al1;
-            acc[mt][2] *= al0;
-            acc[mt][3] *= al1;
-        }
-        // P^T fragments (tokens on K, heads on N) by an in-register transpose
-        const uint32_t pb0 = bi::movmatrix_trans(pA);
-        const uint32_t pb1 = bi::movmatrix_trans(pB);
-        // O^T += V^T . P^T, dims in ascending 16-blocks
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            const int r = lm_r + 8 * (lm_j >> 1);
-            const int ch = 2 * mt + (lm_j & 1);
-            bi::ldmatrix_x4_trans(vs_base + swz(r, ch), a0, a1, a2, a3);
-            bi::mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
-        }
-        // hand the stage back to TMA for this warp's page j + 2
-        bi::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && j + kStagesPerWarp < my_pages) issue(j + kStagesPerWarp);
-    }
-    if (timed_out_at >= 0 && lane == 0) {
-        bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
-        // give this warp's copies still in flight (pages j and j + 1) one more
-        // bounded chance to land before the CTA's shared memory is released
-        for (int j = timed_out_at; j < my_pages && j < timed_out_at + kStagesPerWarp; ++j)
-            (void)bi::mbar_wait(&bars[warp * kStagesPerWarp + (j & 1)], (j >> 1) & 1);
-    }
-    __syncthreads();  // every warp done with the ring: reuse it for the fold
-
-    // per-warp state -> shared: m[8], l[8], acc[8 heads][128 dims]
-    float* wst = reinterpret_cast<float*>(smem) + warp * (2 * kMaxGroup + kMaxGroup * kD);
+    const int lm_j = lane >> 3;  // which 8x8 matrix this lane addresses
+    const int lm_r = lane & 7;   // row within it
     const int h0 = 2 * (lane & 3);
-    if (lane < 4) {
-        wst[h0] = m_run[0];
-        wst[h0 + 1] = m_run[1];
-        wst[kMaxGroup + h0] = l_run[0];
-        wst[kMaxGroup + h0 + 1] = l_run[1];
-    }
-    float* wacc = wst + 2 * kMaxGroup;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        const int d = 16 * mt + (lane >> 2);
-        wacc[h0 * kD + d] = acc[mt][0];
-        wacc[(h0 + 1) * kD + d] = acc[mt][1];
-        wacc[h0 * kD + d + 8] = acc[mt][2];
-        wacc[(h0 + 1) * kD + d + 8] = acc[mt][3];
-    }
-    __syncthreads();
+    const int d = tid;           // output dim this thread owns in the folds
+    float Mr[kMaxGroup], Lr[kMaxGroup], Ar[kMaxGroup];  // running fold over chunks (whole)
+    bool timed_out = false;
+    int j = 0;  // this warp's page counter (matches the loader's)
 
-    // fold warps 0..3 in order; thread = output dim
-    const int d = tid;
-    const float* st0 = reinterpret_cast<const float*>(smem);
-    constexpr int kWarpStride = 2 * kMaxGroup + kMaxGroup * kD;
-    for (int h = 0; h < a.group; ++h) {
-        float M = st0[h];
+    for (int c = c0; c < c1; ++c) {
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_run[2] = {0.f, 0.f};
+        float acc[8][4];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, st0[w * kWarpStride + h]);
-        float Ls = 0.f, A = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float* ws = st0 + w * kWarpStride;
-            const float f = exp2f(ws[h] - M);
-            Ls = __fmaf_rn(ws[kMaxGroup + h], f, Ls);
-            A = __fmaf_rn(ws[2 * kMaxGroup + h * kD + d], f, A);
-        }
-        const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
-        if (nch == 1) {
-            a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(A, Ls));
-        } else {
-            const int64_t pidx = row * a.max_chunks + c;
-            a.ws_acc[pidx * kD + d] = A;
-            if (d == 0) {
-                a.ws_ml[pidx * 2] = M;
-                a.ws_ml[pidx * 2 + 1] = Ls;
+        for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+        const int np = pages_in(c);
+        for (int p = warp; p < np; p += kWarps, ++j) {
+            const int st = warp * kStagesPerWarp + (j & 1);
+            if (timed_out) continue;
+            if (!bi::mbar_wait(&bars[st], (j >> 1) & 1)) {
+                timed_out = true;
+                continue;
             }
+            const uint32_t ks_base = bi::smem_u32(stage_ptr(st));
+            const uint32_t vs_base = ks_base + kMatBytes;
+            const int valid = min(kPage, L - (c * ppc + p) * kPage);
+            if (valid < kPage) {
+                // zero V rows past the sequence end (16-byte units)
+                uint8_t* vd = stage_ptr(st) + kMatBytes;
+                for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
+                    const int r = valid + (idx >> 4), ch = idx & 15;
+                    *reinterpret_cast<uint4*>(vd + swz(r, ch)) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+
+            // S^T = K . Q^T  (tokens on M, heads on N), dims in ascending 16-blocks
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                const int r = lm_r + 8 * (lm_j & 1);
+                const int ch = 2 * ks + (lm_j >> 1);
+                bi::ldmatrix_x4(ks_base + swz(r, ch), a0, a1, a2, a3);
+                bi::mma_bf16_16816(sc, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+            }
+            // sc[0], sc[1]: token lane/4, heads 2(lane%4)+{0,1}; sc[2], sc[3]: token +8
+            const int tokA = lane >> 2, tokB = tokA + 8;
+            const float x0 = tokA < valid ? sc[0] * a.scale_log2 : -INFINITY;
+            const float x1 = tokA < valid ? sc[1] * a.scale_log2 : -INFINITY;
+            const float x2 = tokB < valid ? sc[2] * a.scale_log2 : -INFINITY;
+            const float x3 = tokB < valid ? sc[3] * a.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+            const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+            const uint32_t pA = bi::pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
+            const uint32_t pB = bi::pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
+            // the row sums use the same bf16-rounded weights that multiply V
+            float ps0 = __uint_as_float(pA << 16) + __uint_as_float(pB << 16);
+            float ps1 = __uint_as_float(pA & 0xffff0000u) + __uint_as_float(pB & 0xffff0000u);
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+                ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+            }
+            l_run[0] = __fmaf_rn(l_run[0], al0, ps0);
+            l_run[1] = __fmaf_rn(l_run[1], al1, ps1);
+            m_run[0] = mn0;
+            m_run[1] = mn1;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                acc[mt][0] *= al0;
+                acc[mt][1] *= al1;
+                acc[mt][2] *= al0;
+                acc[mt][3] *= al1;
+            }
+            // P^T fragments (tokens on K, heads on N) by an in-register transpose
+            const uint32_t pb0 = bi::movmatrix_trans(pA);
+            const uint32_t pb1 = bi::movmatrix_trans(pB);
+            // O^T += V^T . P^T, dims in ascending 16-blocks
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                const int r = lm_r + 8 * (lm_j >> 1);
+                const int ch = 2 * mt + (lm_j & 1);
+                bi::ldmatrix_x4_trans(vs_base + swz(r, ch), a0, a1, a2, a3);
+                bi::mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+            // hand the stage back to TMA for this warp's page two ahead
+            bi::fence_proxy_async_smem();
+            __syncwarp();
+            issue_next();
+        }
+
+        // ---- fold the four warp states of chunk c, in warp order 0..3 ----
+        //   M = max_w m_w;  f_w = 2^(m_w - M);
+        //   l = fma(l_3, f_3, fma(l_2, f_2, fma(l_1, f_1, fma(l_0, f_0, 0))))
+        //   O = the same fma chain over the warps' O, which the warps apply
+        //       to one shared [heads][128] buffer one after another.
+        if (lane < 4) {
+            fold_ml[warp * 2 * kMaxGroup + h0] = m_run[0];
+            fold_ml[warp * 2 * kMaxGroup + h0 + 1] = m_run[1];
+            fold_ml[warp * 2 * kMaxGroup + kMaxGroup + h0] = l_run[0];
+            fold_ml[warp * 2 * kMaxGroup + kMaxGroup + h0 + 1] = l_run[1];
+        }
+        __syncthreads();
+        {
+            float Mh0 = fold_ml[h0], Mh1 = fold_ml[h0 + 1];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) {
+                Mh0 = fmaxf(Mh0, fold_ml[w * 2 * kMaxGroup + h0]);
+                Mh1 = fmaxf(Mh1, fold_ml[w * 2 * kMaxGroup + h0 + 1]);
+            }
+            const float f0 = exp2f(m_run[0] - Mh0), f1 = exp2f(m_run[1] - Mh1);
+#pragma unroll 1
+            for (int w = 0; w < kWarps; ++w) {
+                if (warp == w) {
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const int dd = 16 * mt + (lane >> 2);
+                        float* o0 = fold_o + h0 * kD + dd;
+                        float* o1 = fold_o + (h0 + 1) * kD + dd;
+                        const float p00 = w ? o0[0] : 0.f, p10 = w ? o1[0] : 0.f;
+                        const float p01 = w ? o0[8] : 0.f, p11 = w ? o1[8] : 0.f;
+                        o0[0] = __fmaf_rn(acc[mt][0], f0, p00);
+                        o1[0] = __fmaf_rn(acc[mt][1], f1, p10);
+                        o0[8] = __fmaf_rn(acc[mt][2], f0, p01);
+                        o1[8] = __fmaf_rn(acc[mt][3], f1, p11);
+                    }
+                }
+                __syncthreads();
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) {
+            if (h >= a.group) break;
+            float M = fold_ml[h];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) M = fmaxf(M, fold_ml[w * 2 * kMaxGroup + h]);
+            float Ls = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float* ml = fold_ml + w * 2 * kMaxGroup;
+                Ls = __fmaf_rn(ml[kMaxGroup + h], exp2f(ml[h] - M), Ls);
+            }
+            const float A = fold_o[h * kD + d];
+            if (whole) {
+                // the merge kernel's fold, chunk by chunk in ascending order
+                if (c == c0) {
+                    Mr[h] = M;
+                    Lr[h] = Ls;
+                    Ar[h] = A;
+                } else {
+                    const float Mn = fmaxf(Mr[h], M);
+                    const float fo = exp2f(Mr[h] - Mn), fc = exp2f(M - Mn);
+                    Lr[h] = __fmaf_rn(Ls, fc, __fmul_rn(Lr[h], fo));
+                    Ar[h] = __fmaf_rn(A, fc, __fmul_rn(Ar[h], fo));
+                    Mr[h] = Mn;
+                }
+            } else {
+                const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
+                const int64_t pidx = row * a.max_chunks + c;
+                a.ws_acc[pidx * kD + d] = A;
+                if (d == 0) {
+                    a.ws_ml[pidx * 2] = M;
+                    a.ws_ml[pidx * 2 + 1] = Ls;
+                }
+            }
+        }
+        __syncthreads();  // fold area free for the next chunk
+    }
+
+    if (timed_out && lane == 0) bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+    if (whole) {
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) {
+            if (h >= a.group) break;
+            const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
+            a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(Ar[h], Lr[h]));
         }
     }
 }
@@ -336,7 +395,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kD)
     attn_merge_kernel(const int32_t* __restrict__ seq_lens, const float* __restrict__ ws_acc,
                       const float* __restrict__ ws_ml, __nv_bfloat16* __restrict__ out, int Hq,
-                      int max_chunks, int max_seq_len, int num_splits) {
+                      int max_chunks, int max_seq_len, int num_splits, int chunks_per_cta) {
     const int hq = blockIdx.x;
     const int s = blockIdx.y;
     const int d = threadIdx.x;
@@ -344,7 +403,7 @@ __global__ void __launch_bounds__(kD)
     if (L < 1 || L > max_seq_len) return;  // reported by the split kernel
     int ppc, nch;
     chunk_geometry(L, num_splits, ppc, nch);
-    if (nch < 2) return;
+    if (nch <= chunks_per_cta) return;  // one CTA walked and folded every chunk
     const int64_t base = (static_cast<int64_t>(s) * Hq + hq) * max_chunks;
     float M = ws_ml[base * 2];
     float Ls = ws_ml[base * 2 + 1];
@@ -460,12 +519,26 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     args.num_splits = num_splits;
     args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
-    attn_split_kernel<<<dim3(max_chunks, Hkv, B), kThreads, kSmemBytes, stream>>>(tk, tv, args);
+    // Schedule (never the arithmetic): how many consecutive chunks one CTA
+    // walks.  Enough CTAs for about four waves of the resident slots; a
+    // sequence whose chunks all fall to one CTA is folded there, the rest by
+    // the merge kernel -- both apply the same fold in the same chunk order.
+    int cpc = 1;
+    if (num_splits == 0) {
+        const int64_t slots = static_cast<int64_t>(bi::sm_count()) * 3;  // 3 CTAs per SM
+        const int64_t units = static_cast<int64_t>(B) * Hkv * max_chunks;
+        cpc = static_cast<int>(std::min<int64_t>(kMaxChunksPerCta,
+                                                 std::max<int64_t>(1, units / (4 * slots))));
+    }
+    args.chunks_per_cta = cpc;
+    const int groups = ceil_div(max_chunks, cpc);
+
+    attn_split_kernel<<<dim3(groups, Hkv, B), kThreads, kSmemBytes, stream>>>(tk, tv, args);
     if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
-    if (max_chunks >= 2) {
+    if (max_chunks > cpc) {
         attn_merge_kernel<<<dim3(Hq, B), kD, 0, stream>>>(seq_lens, args.ws_acc, args.ws_ml,
                                                           args.out, Hq, max_chunks, max_seq_len,
-                                                          num_splits);
+                                                          num_splits, cpc);
         if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
     }
     return BI_OK;
