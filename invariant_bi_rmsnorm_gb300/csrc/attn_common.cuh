@@ -1,0 +1,155 @@
+// The per-page step of fixed-split-size attention, shared by the decode and
+// prefill kernels so that a query row gets the same bits from either.
+//
+// Arithmetic of one query row (one column) over one 256-token chunk: an online
+// softmax over the chunk's pages 0, 1, 2, ... in order.  For a page of 16
+// tokens (rows of K and V) and 8 columns (query head x query row pairs):
+//     S^T[16 x 8] = K_page[16 x 128] . Q^T[128 x 8]       8 mma.sync, dims ascending
+//     x = S * scale * log2(e)        (tokens past a column's length -> -inf)
+//     m' = max(m, max_t x);  alpha = 2^(m - m');  p = bf16(2^(x - m'))
+//     l' = l * alpha + sum_t p       (fixed xor-butterfly order over tokens)
+//     O^T[128 x 8] = O^T * alpha + V^T[128 x 16] . P^T[16 x 8]   8 mma.sync
+// Each output element of an mma depends only on its own column, so a column's
+// result does not depend on what shares the tile with it.
+//
+// Shared-memory layout of one page block (K or V), as written by two 16 x 64
+// TMA boxes with the 128-byte swizzle: dims [64*(ch/8), +64) at offset
+// (ch/8)*2048, 128-byte rows, the 16-byte unit index XORed with (row % 8).
+#pragma once
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "bi_ptx.cuh"
+
+namespace bi_attn {
+
+constexpr int kD = 128;
+constexpr int kPage = BI_PAGE_SIZE;             // 16 tokens
+constexpr int kChunk = BI_DECODE_CHUNK;         // 256 tokens
+constexpr int kPagesPerChunk = kChunk / kPage;  // 16
+constexpr int kHalfBytes = kPage * 64 * 2;      // 16 rows x 64 dims: one TMA box
+constexpr int kMatBytes = 2 * kHalfBytes;       // one (page, kv-head) K or V block
+constexpr int kStageBytes = 2 * kMatBytes;      // K + V
+constexpr int kMaxGroup = 8;                    // query heads per kv-head
+
+__device__ __forceinline__ uint32_t swz(int r, int ch) {
+    return static_cast<uint32_t>((ch >> 3) * kHalfBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+// Online-softmax state of one warp for 8 columns.  Lane l holds columns
+// 2(l%4) and 2(l%4)+1: m, l for both, and O[d][col] for d = 16mt + l/4 (+8).
+struct ColState {
+    float m[2];
+    float l[2];
+    float acc[8][4];
+};
+
+__device__ __forceinline__ void colstate_init(ColState& st) {
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) st.acc[mt][0] = st.acc[mt][1] = st.acc[mt][2] = st.acc[mt][3] = 0.f;
+}
+
+// Q^T fragments (mma B operand) for the 8 columns: lane l supplies column l/4
+// whose 128-dim query starts at `col_q` (nullptr: a padding column, zeros).
+__device__ __forceinline__ void load_q_frags(const __nv_bfloat16* col_q, int lane, uint32_t (&qb0)[8],
+                                             uint32_t (&qb1)[8]) {
+    const __nv_bfloat16* qp = col_q ? col_q + 2 * (lane & 3) : nullptr;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        qb0[ks] = qp ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks) : 0u;
+        qb1[ks] = qp ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8) : 0u;
+    }
+}
+
+// One page.  valid0 / valid1: how many of the page's 16 tokens columns
+// 2(l%4) and 2(l%4)+1 may see (0 .. 16).  A column that sees none of them
+// keeps its state unchanged.
+__device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint32_t vs_base,
+                                            const uint32_t (&qb0)[8], const uint32_t (&qb1)[8],
+                                            int valid0, int valid1, float scale_log2, int lane) {
+    const int lm_j = lane >> 3;  // which 8x8 matrix this lane addresses
+    const int lm_r = lane & 7;   // row within it
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        bi::ldmatrix_x4(ks_base + swz(lm_r + 8 * (lm_j & 1), 2 * ks + (lm_j >> 1)), a0, a1, a2, a3);
+        bi::mma_bf16_16816(sc, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+    }
+    // sc[0], sc[1]: token l/4, columns 2(l%4)+{0,1}; sc[2], sc[3]: token l/4 + 8
+    const int tokA = lane >> 2, tokB = tokA + 8;
+    const float x0 = tokA < valid0 ? sc[0] * scale_log2 : -INFINITY;
+    const float x1 = tokA < valid1 ? sc[1] * scale_log2 : -INFINITY;
+    const float x2 = tokB < valid0 ? sc[2] * scale_log2 : -INFINITY;
+    const float x3 = tokB < valid1 ? sc[3] * scale_log2 : -INFINITY;
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    // a column with no visible token so far keeps m = -inf: no rescale, p = 0
+    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(st.m[0] - mn0);
+    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(st.m[1] - mn1);
+    const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mn0);
+    const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mn1);
+    const float p2 = x2 == -INFINITY ? 0.f : exp2f(x2 - mn0);
+    const float p3 = x3 == -INFINITY ? 0.f : exp2f(x3 - mn1);
+    const uint32_t pA = bi::pack_bf16x2(p0, p1);
+    const uint32_t pB = bi::pack_bf16x2(p2, p3);
+    // the sums use the same bf16-rounded weights that multiply V
+    float ps0 = __uint_as_float(pA << 16) + __uint_as_float(pB << 16);
+    float ps1 = __uint_as_float(pA & 0xffff0000u) + __uint_as_float(pB & 0xffff0000u);
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+    }
+    st.l[0] = __fmaf_rn(st.l[0], al0, ps0);
+    st.l[1] = __fmaf_rn(st.l[1], al1, ps1);
+    st.m[0] = mn0;
+    st.m[1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        st.acc[mt][0] *= al0;
+        st.acc[mt][1] *= al1;
+        st.acc[mt][2] *= al0;
+        st.acc[mt][3] *= al1;
+    }
+    // P^T fragments (tokens on K, columns on N) by an in-register transpose
+    const uint32_t pb0 = bi::movmatrix_trans(pA);
+    const uint32_t pb1 = bi::movmatrix_trans(pB);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        bi::ldmatrix_x4_trans(vs_base + swz(lm_r + 8 * (lm_j >> 1), 2 * mt + (lm_j & 1)), a0, a1, a2, a3);
+        bi::mma_bf16_16816(st.acc[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+}
+
+// Zero V rows [valid, 16) of a page block in shared memory (one warp).
+__device__ __forceinline__ void zero_v_tail(uint8_t* vd, int valid, int lane) {
+    for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
+        const int r = valid + (idx >> 4), ch = idx & 15;
+        *reinterpret_cast<uint4*>(vd + swz(r, ch)) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Fold step shared by every chunk fold (in-CTA and the merge kernel):
+//   M' = max(M, m_c);  fo = 2^(M - M');  fc = 2^(m_c - M');
+//   l' = fma(l_c, fc, l * fo);  O' = fma(O_c, fc, O * fo).
+__device__ __forceinline__ void fold_scalars(float M, float mc, float& Mn, float& fo, float& fc) {
+    Mn = fmaxf(M, mc);
+    fo = exp2f(M - Mn);
+    fc = exp2f(mc - Mn);
+}
+
+__device__ __forceinline__ float fold_value(float acc, float fo, float part, float fc) {
+    return __fmaf_rn(part, fc, __fmul_rn(acc, fo));
+}
+
+}  // namespace bi_attn

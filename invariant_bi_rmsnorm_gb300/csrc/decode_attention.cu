@@ -8,21 +8,17 @@
 // the KV sequence is split -- but by a fixed split SIZE, so the reduction
 // order of a sequence depends only on its own length.
 //
-// Kernel 1 (split): one CTA per (sequence s, kv-head g, group of consecutive
-// chunks).  Chunk c is tokens [256c, min(256c + 256, L)), i.e. up to 16 pages
-// of 16 tokens.  For each chunk, warp w (of 4) owns the chunk's pages w, w+4,
-// w+8, w+12 and runs an online softmax over them in that order, for the
-// Hq/Hkv query heads that share kv-head g.  Pages arrive by TMA (2-D tiled
-// loads, 128-byte swizzle) into a 2-stage ring per warp that runs on across
-// chunk boundaries.  Per page:
-//     S^T[16 tok x 8 heads] = K_page[16 x 128] . Q^T[128 x 8]   (8 mma.sync)
-//     p = exp2(S * scale * log2 e - m_new), rounded to bf16
-//     O^T[128 x 8] = O^T * alpha + V^T[128 x 16] . P^T[16 x 8]   (8 mma.sync)
-// At the end of each chunk the four warp states are folded in warp order
-// 0..3 into the chunk partial (m, l, O).  If the CTA's group holds every
-// chunk of the sequence, it folds the partials in ascending chunk order with
-// the log-sum-exp rule and writes bf16(O / l); otherwise the partials go to
-// the workspace.
+// Kernel 1 (split): one CTA (4 warps) per (sequence s, kv-head g, group of
+// consecutive chunks).  Chunk c is tokens [256c, min(256c + 256, L)), i.e. up
+// to 16 pages of 16 tokens.  Warp w takes chunks c0 + w, c0 + w + 4, ... of
+// the group and, for the Hq/Hkv query heads sharing kv-head g, runs one online
+// softmax over each chunk's pages 0, 1, 2, ... in order (attn_common.cuh
+// gives the per-page arithmetic).  Pages arrive by TMA (2-D tiled loads,
+// 128-byte swizzle) into a 2-stage ring per warp.  A chunk's final state is its
+// partial (m, l, O).  If the CTA's group holds every chunk of the sequence,
+// the partials are folded in ascending chunk order inside the CTA (warp by
+// warp after each round of four chunks) and bf16(O / l) is written; otherwise
+// the partials go to the workspace.
 // Kernel 2 (merge): for each (sequence, query head) not finished by one CTA,
 // fold the partials in ascending chunk order -- the same fp32 operations in
 // the same order -- and write bf16(O / l).
@@ -39,36 +35,29 @@
 #include <cmath>
 #include <mutex>
 
+#include "attn_common.cuh"
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
 
 namespace {
 
-constexpr int kD = 128;
-constexpr int kPage = BI_PAGE_SIZE;             // 16 tokens
-constexpr int kChunk = BI_DECODE_CHUNK;         // 256 tokens
-constexpr int kPagesPerChunk = kChunk / kPage;  // 16
+using bi_attn::kChunk;
+using bi_attn::kD;
+using bi_attn::kHalfBytes;
+using bi_attn::kMatBytes;
+using bi_attn::kMaxGroup;
+using bi_attn::kPage;
+using bi_attn::kPagesPerChunk;
+using bi_attn::kStageBytes;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStagesPerWarp = 2;
 constexpr int kStages = kWarps * kStagesPerWarp;
-constexpr int kHalfBytes = kPage * 64 * 2;         // 16 rows x 64 dims: one TMA box
-constexpr int kMatBytes = 2 * kHalfBytes;          // one (page, kv-head) K or V block
-constexpr int kStageBytes = 2 * kMatBytes;         // K + V
-constexpr int kMaxGroup = 8;                       // query heads per kv-head (mma N)
-constexpr int kMaxPagesPerCta = 512;                // pages one CTA walks (a chunk group)
+constexpr int kMaxPagesPerCta = 512;                                // pages one CTA walks
 constexpr int kMaxChunksPerCta = kMaxPagesPerCta / kPagesPerChunk;  // 32
-constexpr int kFoldFloats = kMaxGroup * kD + kWarps * 2 * kMaxGroup;  // chunk-fold buffers
+constexpr int kFoldFloats = kMaxGroup * kD + 2 * kMaxGroup;          // running fold (O, M, L)
 constexpr int kSmemBytes = kStages * kStageBytes + kFoldFloats * 4 + 4 * kMaxPagesPerCta +
                            8 * kStages + 1024 /*align*/;  // 71.2 KB: 3 CTAs per SM
-
-// Byte offset of the 16-byte chunk `ch` (0..15) of row `r` (0..15) inside one
-// K or V page block as laid down by two 16x64 TMA boxes with 128-byte
-// swizzle: the box for dims [64*(ch/8), +64) starts at (ch/8)*2048, each row
-// is 128 bytes, and the 16-byte unit index is XORed with (row % 8).
-__device__ __forceinline__ uint32_t swz(int r, int ch) {
-    return static_cast<uint32_t>((ch >> 3) * kHalfBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
-}
 
 struct SplitArgs {
     const __nv_bfloat16* q;
@@ -129,8 +118,9 @@ __global__ void __launch_bounds__(kThreads)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float* fold_o = reinterpret_cast<float*>(smem + kStages * kStageBytes);  // [8 heads][128]
-    float* fold_ml = fold_o + kMaxGroup * kD;                                // [4 warps][m 8, l 8]
-    int32_t* rows_s = reinterpret_cast<int32_t*>(fold_ml + kWarps * 2 * kMaxGroup);  // TMA row per page
+    float* fold_m = fold_o + kMaxGroup * kD;                                // [8]
+    float* fold_l = fold_m + kMaxGroup;                                     // [8]
+    int32_t* rows_s = reinterpret_cast<int32_t*>(fold_l + kMaxGroup);      // TMA row per page
     uint64_t* bars = reinterpret_cast<uint64_t*>(rows_s + kMaxPagesPerCta);
     __shared__ int bad_page;
 
@@ -159,12 +149,11 @@ __global__ void __launch_bounds__(kThreads)
     auto pages_in = [&](int c) { return min(ppc, npg_total - c * ppc); };
     auto stage_ptr = [&](int st) { return smem + st * kStageBytes; };
 
-    // This warp's pages, in order: for each chunk of the group, pages warp,
-    // warp + 4, warp + 8, ... of that chunk.  The loader runs two pages ahead
-    // of the compute loop through a 2-stage ring; every lane tracks the
-    // loader position, lane 0 issues the copies.
-    int lc = c0, lp = warp, lj = 0;
-    while (lc < c1 && lp >= pages_in(lc)) { ++lc; lp = warp; }
+    // This warp's pages, in order: chunk c0 + warp, its pages 0, 1, ...; then
+    // chunk c0 + warp + 4, ...  The loader runs two pages ahead of the compute
+    // loop through this warp's 2-stage ring; every lane tracks the loader
+    // position, lane 0 issues the copies.
+    int lc = c0 + warp, lp = 0, lj = 0;
     auto issue_next = [&]() {
         if (lc >= c1) return;
         if (lane == 0) {
@@ -179,212 +168,128 @@ __global__ void __launch_bounds__(kThreads)
             bi::tma_load_2d(vd + kHalfBytes, &tmap_v, &bars[st], 64, row);
         }
         ++lj;
-        lp += kWarps;
-        while (lc < c1 && lp >= pages_in(lc)) { ++lc; lp = warp; }
+        if (++lp >= pages_in(lc)) {
+            lc += kWarps;
+            lp = 0;
+        }
     };
     issue_next();
     issue_next();
 
-    // Q^T as the mma B operand: lane holds head (lane/4) of the group and
-    // dims 16ks + 2(lane%4) + {0,1} (b0) and +8 (b1).
-    const int qh = lane >> 2;
+    // column n of the mma tile = query head g*group + n (n < group)
     uint32_t qb0[8], qb1[8];
     {
-        const bool valid = qh < a.group;
-        const __nv_bfloat16* qp =
-            a.q + (static_cast<int64_t>(s) * a.Hq + g * a.group + (valid ? qh : 0)) * kD + 2 * (lane & 3);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            qb0[ks] = valid ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks) : 0u;
-            qb1[ks] = valid ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8) : 0u;
-        }
+        const int n = lane >> 2;
+        bi_attn::load_q_frags(
+            n < a.group ? a.q + (static_cast<int64_t>(s) * a.Hq + g * a.group + n) * kD : nullptr,
+            lane, qb0, qb1);
     }
-
-    // ldmatrix lane roles
-    const int lm_j = lane >> 3;  // which 8x8 matrix this lane addresses
-    const int lm_r = lane & 7;   // row within it
     const int h0 = 2 * (lane & 3);
-    const int d = tid;           // output dim this thread owns in the folds
-    float Mr[kMaxGroup], Lr[kMaxGroup], Ar[kMaxGroup];  // running fold over chunks (whole)
     bool timed_out = false;
     int j = 0;  // this warp's page counter (matches the loader's)
+    const int rounds = (c1 - c0 + kWarps - 1) / kWarps;
 
-    for (int c = c0; c < c1; ++c) {
-        float m_run[2] = {-INFINITY, -INFINITY};
-        float l_run[2] = {0.f, 0.f};
-        float acc[8][4];
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-
-        const int np = pages_in(c);
-        for (int p = warp; p < np; p += kWarps, ++j) {
-            const int st = warp * kStagesPerWarp + (j & 1);
-            if (timed_out) continue;
-            if (!bi::mbar_wait(&bars[st], (j >> 1) & 1)) {
-                timed_out = true;
-                continue;
-            }
-            const uint32_t ks_base = bi::smem_u32(stage_ptr(st));
-            const uint32_t vs_base = ks_base + kMatBytes;
-            const int valid = min(kPage, L - (c * ppc + p) * kPage);
-            if (valid < kPage) {
-                // zero V rows past the sequence end (16-byte units)
-                uint8_t* vd = stage_ptr(st) + kMatBytes;
-                for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
-                    const int r = valid + (idx >> 4), ch = idx & 15;
-                    *reinterpret_cast<uint4*>(vd + swz(r, ch)) = make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < rounds; ++r) {
+        const int c = c0 + r * kWarps + warp;  // this warp's chunk in round r
+        bi_attn::ColState st;
+        bi_attn::colstate_init(st);
+        if (c < c1) {
+            const int np = pages_in(c);
+            for (int p = 0; p < np; ++p, ++j) {
+                const int stg = warp * kStagesPerWarp + (j & 1);
+                if (timed_out) continue;
+                if (!bi::mbar_wait(&bars[stg], (j >> 1) & 1)) {
+                    timed_out = true;
+                    continue;
                 }
+                const int valid = min(kPage, L - (c * ppc + p) * kPage);
+                if (valid < kPage) {
+                    bi_attn::zero_v_tail(stage_ptr(stg) + kMatBytes, valid, lane);
+                    __syncwarp();
+                }
+                const uint32_t kb = bi::smem_u32(stage_ptr(stg));
+                bi_attn::attend_page(st, kb, kb + kMatBytes, qb0, qb1, valid, valid, a.scale_log2,
+                                     lane);
+                // hand the stage back to TMA for this warp's page two ahead
+                bi::fence_proxy_async_smem();
                 __syncwarp();
+                issue_next();
             }
-
-            // S^T = K . Q^T  (tokens on M, heads on N), dims in ascending 16-blocks
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (!whole) {
+                // chunk partial -> workspace
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                const int r = lm_r + 8 * (lm_j & 1);
-                const int ch = 2 * ks + (lm_j >> 1);
-                bi::ldmatrix_x4(ks_base + swz(r, ch), a0, a1, a2, a3);
-                bi::mma_bf16_16816(sc, a0, a1, a2, a3, qb0[ks], qb1[ks]);
-            }
-            // sc[0], sc[1]: token lane/4, heads 2(lane%4)+{0,1}; sc[2], sc[3]: token +8
-            const int tokA = lane >> 2, tokB = tokA + 8;
-            const float x0 = tokA < valid ? sc[0] * a.scale_log2 : -INFINITY;
-            const float x1 = tokA < valid ? sc[1] * a.scale_log2 : -INFINITY;
-            const float x2 = tokB < valid ? sc[2] * a.scale_log2 : -INFINITY;
-            const float x3 = tokB < valid ? sc[3] * a.scale_log2 : -INFINITY;
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int off = 4; off <= 16; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-            const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
-            const uint32_t pA = bi::pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
-            const uint32_t pB = bi::pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
-            // the row sums use the same bf16-rounded weights that multiply V
-            float ps0 = __uint_as_float(pA << 16) + __uint_as_float(pB << 16);
-            float ps1 = __uint_as_float(pA & 0xffff0000u) + __uint_as_float(pB & 0xffff0000u);
-#pragma unroll
-            for (int off = 4; off <= 16; off <<= 1) {
-                ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
-                ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
-            }
-            l_run[0] = __fmaf_rn(l_run[0], al0, ps0);
-            l_run[1] = __fmaf_rn(l_run[1], al1, ps1);
-            m_run[0] = mn0;
-            m_run[1] = mn1;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                acc[mt][0] *= al0;
-                acc[mt][1] *= al1;
-                acc[mt][2] *= al0;
-                acc[mt][3] *= al1;
-            }
-            // P^T fragments (tokens on K, heads on N) by an in-register transpose
-            const uint32_t pb0 = bi::movmatrix_trans(pA);
-            const uint32_t pb1 = bi::movmatrix_trans(pB);
-            // O^T += V^T . P^T, dims in ascending 16-blocks
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                const int r = lm_r + 8 * (lm_j >> 1);
-                const int ch = 2 * mt + (lm_j & 1);
-                bi::ldmatrix_x4_trans(vs_base + swz(r, ch), a0, a1, a2, a3);
-                bi::mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
-            }
-            // hand the stage back to TMA for this warp's page two ahead
-            bi::fence_proxy_async_smem();
-            __syncwarp();
-            issue_next();
-        }
-
-        // ---- fold the four warp states of chunk c, in warp order 0..3 ----
-        //   M = max_w m_w;  f_w = 2^(m_w - M);
-        //   l = fma(l_3, f_3, fma(l_2, f_2, fma(l_1, f_1, fma(l_0, f_0, 0))))
-        //   O = the same fma chain over the warps' O, which the warps apply
-        //       to one shared [heads][128] buffer one after another.
-        if (lane < 4) {
-            fold_ml[warp * 2 * kMaxGroup + h0] = m_run[0];
-            fold_ml[warp * 2 * kMaxGroup + h0 + 1] = m_run[1];
-            fold_ml[warp * 2 * kMaxGroup + kMaxGroup + h0] = l_run[0];
-            fold_ml[warp * 2 * kMaxGroup + kMaxGroup + h0 + 1] = l_run[1];
-        }
-        __syncthreads();
-        {
-            float Mh0 = fold_ml[h0], Mh1 = fold_ml[h0 + 1];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) {
-                Mh0 = fmaxf(Mh0, fold_ml[w * 2 * kMaxGroup + h0]);
-                Mh1 = fmaxf(Mh1, fold_ml[w * 2 * kMaxGroup + h0 + 1]);
-            }
-            const float f0 = exp2f(m_run[0] - Mh0), f1 = exp2f(m_run[1] - Mh1);
-#pragma unroll 1
-            for (int w = 0; w < kWarps; ++w) {
-                if (warp == w) {
+                for (int e = 0; e < 2; ++e) {
+                    const int h = h0 + e;
+                    if (h >= a.group) continue;
+                    const int64_t pidx =
+                        (static_cast<int64_t>(s) * a.Hq + g * a.group + h) * a.max_chunks + c;
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
-                        const int dd = 16 * mt + (lane >> 2);
-                        float* o0 = fold_o + h0 * kD + dd;
-                        float* o1 = fold_o + (h0 + 1) * kD + dd;
-                        const float p00 = w ? o0[0] : 0.f, p10 = w ? o1[0] : 0.f;
-                        const float p01 = w ? o0[8] : 0.f, p11 = w ? o1[8] : 0.f;
-                        o0[0] = __fmaf_rn(acc[mt][0], f0, p00);
-                        o1[0] = __fmaf_rn(acc[mt][1], f1, p10);
-                        o0[8] = __fmaf_rn(acc[mt][2], f0, p01);
-                        o1[8] = __fmaf_rn(acc[mt][3], f1, p11);
+                        const int d = 16 * mt + (lane >> 2);
+                        a.ws_acc[pidx * kD + d] = st.acc[mt][e];
+                        a.ws_acc[pidx * kD + d + 8] = st.acc[mt][2 + e];
+                    }
+                    if (lane < 4) {
+                        a.ws_ml[pidx * 2] = st.m[e];
+                        a.ws_ml[pidx * 2 + 1] = st.l[e];
+                    }
+                }
+            }
+        }
+        if (whole) {
+            // fold this round's chunks into the running state, in chunk order
+            for (int w = 0; w < kWarps; ++w) {
+                if (warp == w && c < c1) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = h0 + e;
+                        if (c == 0) {
+#pragma unroll
+                            for (int mt = 0; mt < 8; ++mt) {
+                                const int d = 16 * mt + (lane >> 2);
+                                fold_o[h * kD + d] = st.acc[mt][e];
+                                fold_o[h * kD + d + 8] = st.acc[mt][2 + e];
+                            }
+                        } else {
+                            float Mn, fo, fc;
+                            bi_attn::fold_scalars(fold_m[h], st.m[e], Mn, fo, fc);
+#pragma unroll
+                            for (int mt = 0; mt < 8; ++mt) {
+                                const int d = 16 * mt + (lane >> 2);
+                                float* o = fold_o + h * kD + d;
+                                o[0] = bi_attn::fold_value(o[0], fo, st.acc[mt][e], fc);
+                                o[8] = bi_attn::fold_value(o[8], fo, st.acc[mt][2 + e], fc);
+                            }
+                        }
+                    }
+                    __syncwarp();  // every lane has read M before lanes 0..3 replace it
+                    if (lane < 4) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int h = h0 + e;
+                            if (c == 0) {
+                                fold_m[h] = st.m[e];
+                                fold_l[h] = st.l[e];
+                            } else {
+                                float Mn, fo, fc;
+                                bi_attn::fold_scalars(fold_m[h], st.m[e], Mn, fo, fc);
+                                fold_l[h] = bi_attn::fold_value(fold_l[h], fo, st.l[e], fc);
+                                fold_m[h] = Mn;
+                            }
+                        }
                     }
                 }
                 __syncthreads();
             }
         }
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
-            if (h >= a.group) break;
-            float M = fold_ml[h];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) M = fmaxf(M, fold_ml[w * 2 * kMaxGroup + h]);
-            float Ls = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float* ml = fold_ml + w * 2 * kMaxGroup;
-                Ls = __fmaf_rn(ml[kMaxGroup + h], exp2f(ml[h] - M), Ls);
-            }
-            const float A = fold_o[h * kD + d];
-            if (whole) {
-                // the merge kernel's fold, chunk by chunk in ascending order
-                if (c == c0) {
-                    Mr[h] = M;
-                    Lr[h] = Ls;
-                    Ar[h] = A;
-                } else {
-                    const float Mn = fmaxf(Mr[h], M);
-                    const float fo = exp2f(Mr[h] - Mn), fc = exp2f(M - Mn);
-                    Lr[h] = __fmaf_rn(Ls, fc, __fmul_rn(Lr[h], fo));
-                    Ar[h] = __fmaf_rn(A, fc, __fmul_rn(Ar[h], fo));
-                    Mr[h] = Mn;
-                }
-            } else {
-                const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
-                const int64_t pidx = row * a.max_chunks + c;
-                a.ws_acc[pidx * kD + d] = A;
-                if (d == 0) {
-                    a.ws_ml[pidx * 2] = M;
-                    a.ws_ml[pidx * 2 + 1] = Ls;
-                }
-            }
-        }
-        __syncthreads();  // fold area free for the next chunk
     }
 
     if (timed_out && lane == 0) bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
     if (whole) {
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
-            if (h >= a.group) break;
+        const int d = tid;
+        for (int h = 0; h < a.group; ++h) {
             const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
-            a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(Ar[h], Lr[h]));
+            a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(fold_o[h * kD + d], fold_l[h]));
         }
     }
 }
@@ -412,10 +317,10 @@ __global__ void __launch_bounds__(kD)
         const float mc = ws_ml[(base + c) * 2];
         const float lc = ws_ml[(base + c) * 2 + 1];
         const float ac = ws_acc[(base + c) * kD + d];
-        const float Mn = fmaxf(M, mc);
-        const float fo = exp2f(M - Mn), fc = exp2f(mc - Mn);
-        Ls = __fmaf_rn(lc, fc, __fmul_rn(Ls, fo));
-        A = __fmaf_rn(ac, fc, __fmul_rn(A, fo));
+        float Mn, fo, fc;
+        bi_attn::fold_scalars(M, mc, Mn, fo, fc);
+        Ls = bi_attn::fold_value(Ls, fo, lc, fc);
+        A = bi_attn::fold_value(A, fo, ac, fc);
         M = Mn;
     }
     out[(static_cast<int64_t>(s) * Hq + hq) * kD + d] = __float2bfloat16_rn(__fdiv_rn(A, Ls));
@@ -528,7 +433,11 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
         const int64_t slots = static_cast<int64_t>(bi::sm_count()) * 3;  // 3 CTAs per SM
         const int64_t units = static_cast<int64_t>(B) * Hkv * max_chunks;
         cpc = static_cast<int>(std::min<int64_t>(kMaxChunksPerCta,
-                                                 std::max<int64_t>(1, units / (4 * slots))));
+                                                 std::max<int64_t>(kWarps, units / (4 * slots))));
+    } else {
+        // comparison variant: up to one split per warp, within the page list
+        const int ppc_max = ceil_div(ceil_div(max_seq_len, kPage), num_splits);
+        cpc = std::max(1, std::min(std::min(num_splits, kWarps), kMaxPagesPerCta / ppc_max));
     }
     args.chunks_per_cta = cpc;
     const int groups = ceil_div(max_chunks, cpc);

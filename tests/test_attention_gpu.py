@@ -199,10 +199,14 @@ def test_complete_chunk_partials_stable_as_cache_grows():
         return (f[:acc_elems].view(Hq, max_chunks, D).cpu().numpy().copy(),
                 f[acc_elems:].view(Hq, max_chunks, 2).cpu().numpy().copy())
 
-    a1, m1 = partial_acc(600)   # chunks 0, 1 complete; chunk 2 partial
+    # (a sequence whose chunks all fall to one CTA is folded there and writes
+    # no partials; with one sequence a CTA walks at most 4 chunks, so both
+    # lengths here leave their partials in the workspace)
+    a1, m1 = partial_acc(1100)  # chunks 0..3 complete; chunk 4 partial
     a2, m2 = partial_acc(2048)  # all 8 complete
-    assert np.array_equal(a1[:, :2].view(np.uint32), a2[:, :2].view(np.uint32))
-    assert np.array_equal(m1[:, :2].view(np.uint32), m2[:, :2].view(np.uint32))
+    assert np.isfinite(a1[:, :5]).all() and (m1[:, :5, 1] > 0).all(), "partials not written"
+    assert np.array_equal(a1[:, :4].view(np.uint32), a2[:, :4].view(np.uint32))
+    assert np.array_equal(m1[:, :4].view(np.uint32), m2[:, :4].view(np.uint32))
     # and they agree with the oracle's fp64 chunk partials: m is kept in log2
     # units, so l and O are scaled by 2^(m) / e^(m_oracle)
     _, part = oracle.decode_attention_chunked(**base, chunk=256, max_chunks=max_chunks,
