@@ -186,6 +186,43 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
                               size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * bi_prefill_attention -- many query rows per sequence (a prompt, or one
+ * chunk of it), causal: sequence i's query rows are q rows
+ * q_indptr[i] .. q_indptr[i+1]-1, they are its LAST n_i = q_indptr[i+1] -
+ * q_indptr[i] tokens, and its row j (0-based) attends over the first
+ * seq_lens[i] - n_i + 1 + j cached tokens:
+ *     out[row] = softmax_t( scale * q[row] . k_t[g] ) . v_t[g].
+ *
+ * Operation: "3. Batch-Invariant Attention" of "Defeating Nondeterminism in
+ * LLM Inference: The Core Role of Batch Invariance" (FlashAttention2-style
+ * parallelism over queries, with a reduction order that does not depend on
+ * how many of the sequence's tokens are processed together).  Every row uses
+ * exactly bi_decode_attention's arithmetic for a sequence of its length --
+ * 256-token chunks in order, one online softmax over each chunk's pages in
+ * order, chunk partials folded in order -- so a token's output is
+ * bit-identical whether computed here (whole prompt or any chunking of it) or
+ * by bi_decode_attention.  The caller writes all n_i tokens' K/V into the
+ * cache first.
+ *
+ *   q            device, bf16 [T][Hq][D].   out  device, bf16 [T][Hq][D].
+ *   q_indptr     device, int32 [S + 1], non-decreasing, q_indptr[S] <= T.
+ *   seq_lens     device, int32 [S]: cached tokens of each sequence, including
+ *                its query rows (n_i <= seq_lens[i] <= max_seq_len).
+ *   block_table  device, int32 [S][max_pages_per_seq], as bi_decode_attention.
+ *   max_q_len    host bound on every n_i (sizes the grid).
+ *   S <= 65535; other arguments as bi_decode_attention.  No workspace.
+ * Errors: as bi_decode_attention; an inconsistent q_indptr / seq_lens entry
+ * or an out-of-range page is reported on the device (BI_ERR_DEVICE_BAD_INPUT)
+ * and the affected sequence is skipped.
+ */
+bi_status bi_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, const int32_t* q_indptr, int32_t S,
+                               int32_t T, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                               int32_t num_pages, int32_t max_q_len, int32_t max_seq_len,
+                               float scale, void* out, cudaStream_t stream);
+
+/*
  * bi_decode_attention_fixed_splits -- the same attention with a fixed split
  * COUNT instead of a fixed split size: each sequence's pages are cut into
  * num_splits nearly equal runs (ceil(ceil(L/16)/num_splits) pages each), so

@@ -24,6 +24,7 @@ from . import _lib
 from ._lib import DECODE_CHUNK, PAGE_SIZE
 
 __all__ = ["BiError", "rmsnorm", "gemm", "decode_attention", "decode_attention_fixed_splits",
+           "prefill_attention",
            "decode_attention_workspace_size", "selftest_wait_timeout",
            "decode_num_chunks", "decode_chunk_len", "get_device_error", "abi_version",
            "status_string", "PAGE_SIZE", "DECODE_CHUNK"]
@@ -180,6 +181,46 @@ def decode_attention_fixed_splits(q, k_cache, v_cache, block_table, seq_lens, ma
         block_table.shape[1], seq_lens.data_ptr(), B, Hq, Hkv, D, page, num_pages,
         int(max_seq_len), float(scale), int(num_splits), out.data_ptr(), ws_ptr, ws_bytes,
         _stream(stream)), "bi_decode_attention_fixed_splits")
+    return out
+
+
+def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor, q_indptr: torch.Tensor,
+                      max_q_len: int, max_seq_len: int, scale: float | None = None,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal attention for the last n_i tokens of each sequence at once.
+
+    q [T, Hq, D]; q_indptr [S + 1] int32 (sequence i owns q rows
+    q_indptr[i] .. q_indptr[i+1]-1); seq_lens [S] int32 (cached tokens,
+    including the query rows); block_table [S, max_pages_per_seq] int32.
+    Bit-identical per row to decode_attention with the row's own length."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _cuda_bf16(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens"), (q_indptr, "q_indptr")):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("prefill_attention: q [T,Hq,D] and caches [P,Hkv,page,D] expected")
+    T, Hq, D = q.shape
+    num_pages, Hkv, page, D2 = k_cache.shape
+    S = seq_lens.shape[0]
+    if (D2 != D or block_table.dim() != 2 or block_table.shape[0] != S
+            or tuple(q_indptr.shape) != (S + 1,)):
+        raise ValueError("prefill_attention: inconsistent shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _cuda_bf16(out, "out")
+    if tuple(out.shape) != (T, Hq, D) or not out.is_contiguous():
+        raise ValueError("prefill_attention: out must be a contiguous [T, Hq, D] tensor")
+    _check(_lib.load().bi_prefill_attention(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+        block_table.shape[1], seq_lens.data_ptr(), q_indptr.data_ptr(), S, T, Hq, Hkv, D, page,
+        num_pages, int(max_q_len), int(max_seq_len), float(scale), out.data_ptr(),
+        _stream(stream)), "bi_prefill_attention")
     return out
 
 

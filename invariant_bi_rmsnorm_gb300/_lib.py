@@ -28,7 +28,7 @@ EXPORTS = (
     "bi_abi_version", "bi_status_string", "bi_get_device_error", "bi_rmsnorm", "bi_gemm",
     "bi_decode_attention_workspace_size", "bi_decode_num_chunks", "bi_decode_chunk_len",
     "bi_decode_attention", "bi_decode_attention_noalloc", "bi_decode_attention_fixed_splits",
-    "bi_selftest_wait_timeout",
+    "bi_selftest_wait_timeout", "bi_prefill_attention",
 )
 
 _lib = None
@@ -75,6 +75,10 @@ def load() -> ctypes.CDLL:
         _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
         _i32, _vp, _vp, ctypes.c_size_t, _vp]
     lib.bi_decode_attention_fixed_splits.restype = ctypes.c_int
+    lib.bi_prefill_attention.argtypes = [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
+                                         _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _vp,
+                                         _vp]
+    lib.bi_prefill_attention.restype = ctypes.c_int
     lib.bi_selftest_wait_timeout.argtypes = [_i32, _vp]
     lib.bi_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
