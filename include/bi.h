@@ -98,6 +98,19 @@ bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int32_
                      int64_t ld_x, int64_t ld_y, float eps, cudaStream_t stream);
 
 /*
+ * bi_add_rmsnorm -- the residual add fused with the RMSNorm that follows it:
+ *     residual[r][i] = bf16(residual[r][i] + x[r][i])      (written back)
+ *     y[r][i]        = RMSNorm(residual[r])[i] * w[i]        as bi_rmsnorm
+ * bit-identical to an elementwise add followed by bi_rmsnorm, in one pass.
+ * Pointwise adds are batch-invariant ("Achieving Batch-Invariant Kernels");
+ * the reduction is bi_rmsnorm's.  y must not overlap residual or x.
+ * Arguments and errors as bi_rmsnorm, plus residual [rows][ld_res].
+ */
+bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y, int64_t rows,
+                         int32_t hidden, int64_t ld_x, int64_t ld_res, int64_t ld_y, float eps,
+                         cudaStream_t stream);
+
+/*
  * bi_gemm -- y[M][N] = bf16( x[M][K] . W[N][K]^T ), fp32 accumulation.
  *
  * Operation: "2. Batch-Invariant Matrix Multiplication" of the same page: a
@@ -221,6 +234,47 @@ bi_status bi_prefill_attention(const void* q, const void* k_cache, const void* v
                                int32_t T, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
                                int32_t num_pages, int32_t max_q_len, int32_t max_seq_len,
                                float scale, void* out, cudaStream_t stream);
+
+/*
+ * bi_qk_norm_rope_append -- the steps between the qkv projection and
+ * attention, for T new tokens: per-head RMSNorm of q and k (when a weight is
+ * given), rotary position embedding (rotate-half pairing of dims i and
+ * 64 + i), q written out, k and v appended into the paged cache.
+ *
+ *   qkv        device, bf16 [T][ld_qkv]: per token Hq q-heads, then Hkv
+ *              k-heads, then Hkv v-heads, 128 values each.
+ *   positions  device, int32 [T]: each token's position (0 .. max_pos-1).
+ *   slots      device, int32 [T]: each token's cache slot, page * 16 + offset.
+ *   rope_table device, fp32 [max_pos][128]: cos(pos * f_i) at i and
+ *              sin(pos * f_i) at 64 + i, i < 64 (f_i = theta^(-i/64)).
+ *   q_norm_w, k_norm_w  device, bf16 [128], or null for no per-head norm.
+ *   q_out      device, bf16 [T][Hq][128].
+ *   k_cache, v_cache    as bi_decode_attention, num_pages pages.
+ * Per head: x -> bf16(x * rsqrt(mean(x^2) + eps) * w) (fp32, sum of squares
+ * in an order fixed by the head size) -> y_i = x_i c - x_{64+i} s,
+ * y_{64+i} = x_{64+i} c + x_i s in fp32, rounded once to bf16.  Pointwise
+ * and per-head, hence batch-invariant ("Achieving Batch-Invariant Kernels");
+ * the append is the "3. Batch-Invariant Attention" rule that new tokens join
+ * the one cache layout before attention reads it.  D = 128, page_size = 16.
+ * A position or slot out of range is reported on the device
+ * (BI_ERR_DEVICE_BAD_INPUT) and that token is skipped.
+ */
+bi_status bi_qk_norm_rope_append(const void* qkv, int64_t ld_qkv, int32_t T, int32_t Hq,
+                                 int32_t Hkv, int32_t D, const int32_t* positions,
+                                 const int32_t* slots, const float* rope_table, int32_t max_pos,
+                                 const void* q_norm_w, const void* k_norm_w, float eps,
+                                 void* q_out, void* k_cache, void* v_cache, int32_t num_pages,
+                                 int32_t page_size, cudaStream_t stream);
+
+/*
+ * bi_silu_mul -- the SwiGLU product: out[t][j] = bf16(silu(g) * u) with
+ * g = gate_up[t][j], u = gate_up[t][F + j], silu(g) = g / (1 + exp(-g)), all
+ * in fp32.  Pointwise, hence batch-invariant.  F a multiple of 8.
+ *   gate_up  device, bf16 [T][ld_gate_up] (gate columns 0..F-1, up F..2F-1).
+ *   out      device, bf16 [T][ld_out].
+ */
+bi_status bi_silu_mul(const void* gate_up, int64_t ld_gate_up, int32_t T, int32_t F, void* out,
+                      int64_t ld_out, cudaStream_t stream);
 
 /*
  * bi_decode_attention_fixed_splits -- the same attention with a fixed split

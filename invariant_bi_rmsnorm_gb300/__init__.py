@@ -24,7 +24,8 @@ from . import _lib
 from ._lib import DECODE_CHUNK, PAGE_SIZE
 
 __all__ = ["BiError", "rmsnorm", "gemm", "decode_attention", "decode_attention_fixed_splits",
-           "prefill_attention",
+           "prefill_attention", "add_rmsnorm", "qk_norm_rope_append", "silu_mul",
+           "rope_table",
            "decode_attention_workspace_size", "selftest_wait_timeout",
            "decode_num_chunks", "decode_chunk_len", "get_device_error", "abi_version",
            "status_string", "PAGE_SIZE", "DECODE_CHUNK"]
@@ -100,6 +101,78 @@ def rmsnorm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, out: torch.Tens
     ld_y = _row_major_2d(out, "out")
     _check(_lib.load().bi_rmsnorm(x.data_ptr(), w.data_ptr(), out.data_ptr(), rows, hidden,
                                   ld_x, ld_y, float(eps), _stream(stream)), "bi_rmsnorm")
+    return out
+
+
+def add_rmsnorm(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: float = 1e-6,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """residual += x (bf16, in place), then RMSNorm(residual) * w -> out."""
+    for t, n in ((x, "x"), (residual, "residual"), (w, "w")):
+        _cuda_bf16(t, n)
+    if x.shape != residual.shape or x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1]:
+        raise ValueError("add_rmsnorm: x, residual [rows, hidden] and w [hidden] expected")
+    rows, hidden = x.shape
+    if out is None:
+        out = torch.empty((rows, hidden), dtype=torch.bfloat16, device=x.device)
+    _cuda_bf16(out, "out")
+    _check(_lib.load().bi_add_rmsnorm(x.data_ptr(), residual.data_ptr(), w.data_ptr(),
+                                      out.data_ptr(), rows, hidden, _row_major_2d(x, "x"),
+                                      _row_major_2d(residual, "residual"),
+                                      _row_major_2d(out, "out"), float(eps), _stream(stream)),
+           "bi_add_rmsnorm")
+    return out
+
+
+def rope_table(max_pos: int, theta: float, D: int = 128, device=None) -> torch.Tensor:
+    """fp32 [max_pos][D] table: cos(pos * f_i) at i and sin(pos * f_i) at D/2 + i,
+    f_i = theta^(-i/(D/2)), evaluated in float64 on the host and rounded once."""
+    half = D // 2
+    pos = torch.arange(max_pos, dtype=torch.float64)[:, None]
+    f = torch.pow(torch.tensor(float(theta), dtype=torch.float64),
+                  -torch.arange(half, dtype=torch.float64) / half)[None, :]
+    ang = pos * f
+    tab = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+    return tab.to(device) if device is not None else tab
+
+
+def qk_norm_rope_append(qkv: torch.Tensor, Hq: int, Hkv: int, positions: torch.Tensor,
+                        slots: torch.Tensor, rope: torch.Tensor, q_norm_w, k_norm_w,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, eps: float = 1e-6,
+                        q_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per-head q/k RMSNorm + RoPE; q -> q_out [T, Hq, 128]; k, v -> cache slots."""
+    _cuda_bf16(qkv, "qkv")
+    T = qkv.shape[0]
+    D = 128
+    if q_out is None:
+        q_out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=qkv.device)
+    for t, n in ((positions, "positions"), (slots, "slots")):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous() or t.shape[0] != T:
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor of length T")
+    if not rope.is_cuda or rope.dtype != torch.float32 or not rope.is_contiguous():
+        raise ValueError("rope must be a contiguous float32 CUDA tensor")
+    num_pages, Hkv2, page, D2 = k_cache.shape
+    if Hkv2 != Hkv or D2 != D:
+        raise ValueError("qk_norm_rope_append: cache shape mismatch")
+    _check(_lib.load().bi_qk_norm_rope_append(
+        qkv.data_ptr(), _row_major_2d(qkv, "qkv"), T, Hq, Hkv, D, positions.data_ptr(),
+        slots.data_ptr(), rope.data_ptr(), rope.shape[0],
+        q_norm_w.data_ptr() if q_norm_w is not None else None,
+        k_norm_w.data_ptr() if k_norm_w is not None else None, float(eps), q_out.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), num_pages, page, _stream(stream)),
+        "bi_qk_norm_rope_append")
+    return q_out
+
+
+def silu_mul(gate_up: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """SwiGLU: out = silu(gate_up[:, :F]) * gate_up[:, F:]."""
+    _cuda_bf16(gate_up, "gate_up")
+    T, F2 = gate_up.shape
+    F = F2 // 2
+    if out is None:
+        out = torch.empty((T, F), dtype=torch.bfloat16, device=gate_up.device)
+    _check(_lib.load().bi_silu_mul(gate_up.data_ptr(), _row_major_2d(gate_up, "gate_up"), T, F,
+                                   out.data_ptr(), _row_major_2d(out, "out"), _stream(stream)),
+           "bi_silu_mul")
     return out
 
 

@@ -28,7 +28,8 @@ EXPORTS = (
     "bi_abi_version", "bi_status_string", "bi_get_device_error", "bi_rmsnorm", "bi_gemm",
     "bi_decode_attention_workspace_size", "bi_decode_num_chunks", "bi_decode_chunk_len",
     "bi_decode_attention", "bi_decode_attention_noalloc", "bi_decode_attention_fixed_splits",
-    "bi_selftest_wait_timeout", "bi_prefill_attention",
+    "bi_selftest_wait_timeout", "bi_prefill_attention", "bi_add_rmsnorm",
+    "bi_qk_norm_rope_append", "bi_silu_mul",
 )
 
 _lib = None
@@ -79,6 +80,15 @@ def load() -> ctypes.CDLL:
                                          _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _vp,
                                          _vp]
     lib.bi_prefill_attention.restype = ctypes.c_int
+    lib.bi_add_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _i64, _i64, _i64,
+                                   ctypes.c_float, _vp]
+    lib.bi_add_rmsnorm.restype = ctypes.c_int
+    lib.bi_qk_norm_rope_append.argtypes = [_vp, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32,
+                                           _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i32, _i32,
+                                           _vp]
+    lib.bi_qk_norm_rope_append.restype = ctypes.c_int
+    lib.bi_silu_mul.argtypes = [_vp, _i64, _i32, _i32, _vp, _i64, _vp]
+    lib.bi_silu_mul.restype = ctypes.c_int
     lib.bi_selftest_wait_timeout.argtypes = [_i32, _vp]
     lib.bi_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib

@@ -22,7 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libbi.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["api.cu", "rmsnorm.cu", "gemm.cu", "decode_attention.cu", "prefill_attention.cu"]
+SOURCES = ["api.cu", "rmsnorm.cu", "gemm.cu", "decode_attention.cu", "prefill_attention.cu",
+           "decoder_ops.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

@@ -28,6 +28,7 @@ enum : uint32_t {
     kWhereAttnSplit = 5u << 8,
     kWhereAttnMerge = 6u << 8,
     kWhereSelftest = 7u << 8,
+    kWhereDecoderOps = 8u << 8,
 };
 
 // Device address of the current device's error word (nullptr on failure).

@@ -1,0 +1,203 @@
+// Pointwise and per-head steps a decoder layer needs around the three
+// reduction kernels: per-head q/k RMSNorm + rotary embedding + append of the
+// new tokens' K/V into the paged cache, and the SwiGLU product.
+//
+// "Defeating Nondeterminism in LLM Inference: The Core Role of Batch
+// Invariance", section "Achieving Batch-Invariant Kernels": pointwise
+// operations are batch-invariant by construction; the per-head RMSNorm here
+// reduces over one head's 128 values in an order fixed by the head size.  The
+// KV append follows "3. Batch-Invariant Attention": the new tokens' K/V go
+// into the same paged cache as every earlier token before attention runs.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kHalf = kD / 2;
+constexpr int kWarpsPerBlock = 4;
+
+__device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
+
+struct RopeArgs {
+    const __nv_bfloat16* qkv;
+    int64_t ld_qkv;
+    int T, Hq, Hkv;
+    const int32_t* positions;
+    const int32_t* slots;
+    const float* rope;  // [max_pos][128]: cos(pos * f_i) at i, sin(pos * f_i) at 64 + i
+    int max_pos;
+    const __nv_bfloat16* q_norm_w;  // [128] or null
+    const __nv_bfloat16* k_norm_w;  // [128] or null
+    float eps;
+    __nv_bfloat16* q_out;  // [T][Hq][128]
+    __nv_bfloat16* k_cache;
+    __nv_bfloat16* v_cache;  // [num_pages][Hkv][16][128]
+    int64_t num_slots;       // num_pages * 16
+    int page_size;
+    uint32_t* err;
+};
+
+// One warp per (token, head).  Lane l holds dims 2l, 2l+1 (first half) and
+// 64+2l, 64+2l+1 (their rotation partners).
+//   q, k heads:  x -> bf16(x * rsqrt(mean(x^2) + eps) * w)   (if a norm weight is given;
+//                    sum of squares: per lane in the order 2l, 2l+1, 64+2l, 64+2l+1, then
+//                    an xor butterfly over lanes)
+//                -> rotate-half RoPE in fp32: y_i = x_i c_i - x_{64+i} s_i,
+//                   y_{64+i} = x_{64+i} c_i + x_i s_i, rounded once to bf16
+//   v heads:     copied.
+// q goes to q_out; k and v to their token's cache slot.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) qk_norm_rope_append_kernel(const RopeArgs a) {
+    const int warp_global = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int heads = a.Hq + 2 * a.Hkv;
+    if (warp_global >= a.T * heads) return;
+    const int t = warp_global / heads;
+    const int h = warp_global % heads;
+    const int pos = a.positions[t];
+    const int64_t slot = a.slots[t];
+    if (pos < 0 || pos >= a.max_pos || slot < 0 || slot >= a.num_slots) {
+        if (lane == 0 && h == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereDecoderOps);
+        return;
+    }
+    const __nv_bfloat16* src = a.qkv + static_cast<int64_t>(t) * a.ld_qkv + static_cast<int64_t>(h) * kD;
+    const int i0 = 2 * lane;
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(src + i0);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(src + kHalf + i0);
+    float x[4] = {__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi)};
+
+    const int64_t page = slot / a.page_size, off = slot % a.page_size;
+    if (h >= a.Hq + a.Hkv) {  // v: copy into the cache
+        const int hv = h - a.Hq - a.Hkv;
+        __nv_bfloat16* dst = a.v_cache + ((page * a.Hkv + hv) * a.page_size + off) * kD;
+        *reinterpret_cast<__nv_bfloat162*>(dst + i0) = lo;
+        *reinterpret_cast<__nv_bfloat162*>(dst + kHalf + i0) = hi;
+        return;
+    }
+    const bool is_q = h < a.Hq;
+    const __nv_bfloat16* nw = is_q ? a.q_norm_w : a.k_norm_w;
+    if (nw) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ss = __fmaf_rn(x[e], x[e], ss);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(__fdiv_rn(ss, static_cast<float>(kD)) + a.eps);
+        const int idx[4] = {i0, i0 + 1, kHalf + i0, kHalf + i0 + 1};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            x[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(x[e], r), bf(nw[idx[e]]))));
+    }
+    const float* cs = a.rope + static_cast<int64_t>(pos) * kD;
+    float y[4];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const float c = cs[i0 + e], sn = cs[kHalf + i0 + e];
+        y[e] = __fsub_rn(__fmul_rn(x[e], c), __fmul_rn(x[2 + e], sn));
+        y[2 + e] = __fadd_rn(__fmul_rn(x[2 + e], c), __fmul_rn(x[e], sn));
+    }
+    __nv_bfloat16* dst;
+    if (is_q) {
+        dst = a.q_out + (static_cast<int64_t>(t) * a.Hq + h) * kD;
+    } else {
+        const int hk = h - a.Hq;
+        dst = a.k_cache + ((page * a.Hkv + hk) * a.page_size + off) * kD;
+    }
+    *reinterpret_cast<__nv_bfloat162*>(dst + i0) = __floats2bfloat162_rn(y[0], y[1]);
+    *reinterpret_cast<__nv_bfloat162*>(dst + kHalf + i0) = __floats2bfloat162_rn(y[2], y[3]);
+}
+
+// h[t][j] = bf16( silu(g) * u ),  g = gu[t][j], u = gu[t][F + j],
+// silu(g) = g / (1 + exp(-g)), all in fp32.  8 outputs per thread.
+__global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_gu,
+                                __nv_bfloat16* __restrict__ out, int64_t ld_out, int T, int F) {
+    const int64_t nvec = static_cast<int64_t>(T) * (F / 8);
+    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < nvec;
+         v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = v / (F / 8);
+        const int j = static_cast<int>(v % (F / 8)) * 8;
+        const uint4 gv = *reinterpret_cast<const uint4*>(gu + t * ld_gu + j);
+        const uint4 uv = *reinterpret_cast<const uint4*>(gu + t * ld_gu + F + j);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+        const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uv);
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float ga = __low2float(g2[e]), gb = __high2float(g2[e]);
+            const float sa = __fdiv_rn(ga, __fadd_rn(1.f, expf(-ga)));
+            const float sb = __fdiv_rn(gb, __fadd_rn(1.f, expf(-gb)));
+            o[e] = bi::pack_bf16x2(__fmul_rn(sa, __low2float(u2[e])), __fmul_rn(sb, __high2float(u2[e])));
+        }
+        *reinterpret_cast<uint4*>(out + t * ld_out + j) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+}  // namespace
+
+extern "C" bi_status bi_qk_norm_rope_append(const void* qkv, int64_t ld_qkv, int32_t T, int32_t Hq,
+                                            int32_t Hkv, int32_t D, const int32_t* positions,
+                                            const int32_t* slots, const float* rope_table,
+                                            int32_t max_pos, const void* q_norm_w,
+                                            const void* k_norm_w, float eps, void* q_out,
+                                            void* k_cache, void* v_cache, int32_t num_pages,
+                                            int32_t page_size, cudaStream_t stream) {
+    if (T < 0 || Hq <= 0 || Hkv <= 0 || max_pos < 1 || num_pages < 1) return BI_ERR_INVALID_ARG;
+    if (D != kD || page_size != BI_PAGE_SIZE) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (ld_qkv < static_cast<int64_t>(Hq + 2 * Hkv) * kD) return BI_ERR_INVALID_ARG;
+    if (ld_qkv & 7) return BI_ERR_MISALIGNED;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return BI_ERR_INVALID_ARG;
+    if (T == 0) return BI_OK;
+    if (!qkv || !positions || !slots || !rope_table || !q_out || !k_cache || !v_cache)
+        return BI_ERR_INVALID_ARG;
+    if (!bi::aligned16(qkv) || !bi::aligned16(q_out) || !bi::aligned16(k_cache) ||
+        !bi::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(rope_table) & 15) ||
+        (reinterpret_cast<uintptr_t>(positions) & 3) || (reinterpret_cast<uintptr_t>(slots) & 3))
+        return BI_ERR_MISALIGNED;
+    RopeArgs a;
+    a.qkv = static_cast<const __nv_bfloat16*>(qkv);
+    a.ld_qkv = ld_qkv;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.positions = positions;
+    a.slots = slots;
+    a.rope = rope_table;
+    a.max_pos = max_pos;
+    a.q_norm_w = static_cast<const __nv_bfloat16*>(q_norm_w);
+    a.k_norm_w = static_cast<const __nv_bfloat16*>(k_norm_w);
+    a.eps = eps;
+    a.q_out = static_cast<__nv_bfloat16*>(q_out);
+    a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+    a.num_slots = static_cast<int64_t>(num_pages) * page_size;
+    a.page_size = page_size;
+    a.err = bi::device_error_word();
+    const int64_t warps = static_cast<int64_t>(T) * (Hq + 2 * Hkv);
+    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffffLL) return BI_ERR_UNSUPPORTED_SHAPE;
+    qk_norm_rope_append_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+extern "C" bi_status bi_silu_mul(const void* gate_up, int64_t ld_gate_up, int32_t T, int32_t F,
+                                 void* out, int64_t ld_out, cudaStream_t stream) {
+    if (T < 0 || F < 8 || (F & 7)) return T < 0 ? BI_ERR_INVALID_ARG : BI_ERR_UNSUPPORTED_SHAPE;
+    if (ld_gate_up < 2 * static_cast<int64_t>(F) || ld_out < F) return BI_ERR_INVALID_ARG;
+    if ((ld_gate_up & 7) || (ld_out & 7)) return BI_ERR_MISALIGNED;
+    if (T == 0) return BI_OK;
+    if (!gate_up || !out) return BI_ERR_INVALID_ARG;
+    if (!bi::aligned16(gate_up) || !bi::aligned16(out)) return BI_ERR_MISALIGNED;
+    const int64_t nvec = static_cast<int64_t>(T) * (F / 8);
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((nvec + threads - 1) / threads,
+                                             static_cast<int64_t>(bi::sm_count()) * 16);
+    silu_mul_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), threads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(gate_up), ld_gate_up, static_cast<__nv_bfloat16*>(out),
+        ld_out, T, F);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}

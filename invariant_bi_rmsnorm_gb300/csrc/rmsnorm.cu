@@ -30,10 +30,13 @@ constexpr int kMaxThreads = 256;
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-template <int VPT>
+// kAdd: the fused form -- first res = bf16(res + x) (fp32 add, one rounding),
+// stored back, then the RMSNorm of that sum with exactly the reduction below.
+template <int VPT, bool kAdd>
 __global__ void __launch_bounds__(kMaxThreads)
     rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloat16* __restrict__ w, __nv_bfloat16* y,
-                   int hidden, int64_t ld_x, int64_t ld_y, float eps) {
+                   int hidden, int64_t ld_x, int64_t ld_y, float eps, __nv_bfloat16* res,
+                   int64_t ld_res) {
     __shared__ float warp_sums[kMaxThreads / 32];
     const int nvec = hidden >> 3;
     const int tid = threadIdx.x;
@@ -47,6 +50,24 @@ __global__ void __launch_bounds__(kMaxThreads)
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + j * T;
         xv[j] = (v < nvec) ? __ldcs(xr + v) : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (kAdd) {
+        uint4* rr = reinterpret_cast<uint4*>(res + row * ld_res);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + j * T;
+            if (v >= nvec) continue;
+            const uint4 rv = rr[v];
+            const uint32_t xu[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+            const uint32_t ru[4] = {rv.x, rv.y, rv.z, rv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o[e] = bi::pack_bf16x2(__fadd_rn(bf16_lo(ru[e]), bf16_lo(xu[e])),
+                                       __fadd_rn(bf16_hi(ru[e]), bf16_hi(xu[e])));
+            xv[j] = make_uint4(o[0], o[1], o[2], o[3]);
+            rr[v] = xv[j];
+        }
     }
 
     float s = 0.f;
@@ -90,17 +111,24 @@ __global__ void __launch_bounds__(kMaxThreads)
 
 }  // namespace
 
-extern "C" bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t rows,
-                                int32_t hidden, int64_t ld_x, int64_t ld_y, float eps,
-                                cudaStream_t stream) {
+namespace {
+
+template <bool kAdd>
+bi_status launch_rmsnorm(const void* x, const void* w, void* y, int64_t rows, int32_t hidden,
+                         int64_t ld_x, int64_t ld_y, float eps, void* res, int64_t ld_res,
+                         cudaStream_t stream) {
     if (rows < 0 || rows > 0x7fffffffLL) return BI_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || eps != eps || eps > 3.0e38f) return BI_ERR_INVALID_ARG;
     if (hidden < 8 || hidden > 32768 || (hidden & 7)) return BI_ERR_UNSUPPORTED_SHAPE;
     if (ld_x < hidden || ld_y < hidden) return BI_ERR_INVALID_ARG;
     if ((ld_x & 7) || (ld_y & 7)) return BI_ERR_MISALIGNED;
+    if (kAdd && ld_res < hidden) return BI_ERR_INVALID_ARG;
+    if (kAdd && (ld_res & 7)) return BI_ERR_MISALIGNED;
     if (rows == 0) return BI_OK;
-    if (!x || !w || !y) return BI_ERR_INVALID_ARG;
-    if (!bi::aligned16(x) || !bi::aligned16(w) || !bi::aligned16(y)) return BI_ERR_MISALIGNED;
+    if (!x || !w || !y || (kAdd && !res)) return BI_ERR_INVALID_ARG;
+    if (!bi::aligned16(x) || !bi::aligned16(w) || !bi::aligned16(y) ||
+        (kAdd && !bi::aligned16(res)))
+        return BI_ERR_MISALIGNED;
 
     // Thread count and vectors per thread depend on `hidden` alone.
     const int nvec = hidden / 8;
@@ -115,16 +143,31 @@ extern "C" bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t r
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* wb = static_cast<const __nv_bfloat16*>(w);
     auto* yb = static_cast<__nv_bfloat16*>(y);
+    auto* rb = static_cast<__nv_bfloat16*>(res);
     const dim3 grid(static_cast<unsigned>(rows));
     if (vpt == 1)
-        rmsnorm_kernel<1><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+        rmsnorm_kernel<1, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res);
     else if (vpt == 2)
-        rmsnorm_kernel<2><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+        rmsnorm_kernel<2, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res);
     else if (vpt <= 4)
-        rmsnorm_kernel<4><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+        rmsnorm_kernel<4, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res);
     else if (vpt <= 8)
-        rmsnorm_kernel<8><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+        rmsnorm_kernel<8, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res);
     else
-        rmsnorm_kernel<16><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps);
+        rmsnorm_kernel<16, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t rows,
+                                int32_t hidden, int64_t ld_x, int64_t ld_y, float eps,
+                                cudaStream_t stream) {
+    return launch_rmsnorm<false>(x, w, y, rows, hidden, ld_x, ld_y, eps, nullptr, hidden, stream);
+}
+
+extern "C" bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y,
+                                    int64_t rows, int32_t hidden, int64_t ld_x, int64_t ld_res,
+                                    int64_t ld_y, float eps, cudaStream_t stream) {
+    return launch_rmsnorm<true>(x, w, y, rows, hidden, ld_x, ld_y, eps, residual, ld_res, stream);
 }

@@ -1,0 +1,290 @@
+"""A random-init Qwen3-8B-shaped decoder served with continuous batching on the
+batch-invariant kernels.
+
+Every reduction of the forward pass runs in this library's kernels (RMSNorm,
+GEMM, prefill and decode attention), and so do the per-token steps around
+them (per-head q/k norm + RoPE + paged KV append, SwiGLU, residual add fused
+with RMSNorm).  The only torch operations are the embedding-row gather and the
+final argmax, both exact.  So a request's logits are bit-identical whatever
+else shares its step -- the property "Defeating Nondeterminism in LLM
+Inference: The Core Role of Batch Invariance" ("Experimental Validation")
+demonstrates end to end, here on random weights instead of a trained model.
+
+Scheduler: each step takes every running sequence's next token (decode), then
+fills the rest of a per-step token budget with prompt tokens of waiting
+sequences -- a prompt that does not fit is split across steps (chunked
+prefill).  Decode rows use bi_decode_attention; prompt rows use
+bi_prefill_attention; both give a token the same bits.
+"""
+from __future__ import annotations
+
+import math
+from collections import deque
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import (add_rmsnorm, decode_attention, decode_attention_workspace_size, gemm,
+               prefill_attention, qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
+from . import inputs
+from ._lib import PAGE_SIZE
+
+
+@dataclass
+class Qwen3Config:
+    hidden: int = 4096
+    layers: int = 36
+    ffn: int = 12288
+    heads: int = 32
+    kv_heads: int = 8
+    head_dim: int = 128
+    vocab: int = 151936
+    rope_theta: float = 1e6
+    eps: float = 1e-6
+    max_pos: int = 8192
+
+
+class Qwen3Weights:
+    """Seeded random-init weights on the device: linear layers ~ N(0, 0.02)
+    in the nn.Linear [out, in] layout, norm weights 1 (q/k norms included),
+    untied embedding and lm_head."""
+
+    def __init__(self, cfg: Qwen3Config, seed: int = 1000, device="cuda"):
+        self.cfg = cfg
+        H, F, D = cfg.hidden, cfg.ffn, cfg.head_dim
+        qkv_out = (cfg.heads + 2 * cfg.kv_heads) * D
+        w = lambda shape, k: inputs.normal_bf16(shape, seed + k, std=0.02, device=device)  # noqa: E731
+        ones = lambda n: torch.ones(n, dtype=torch.bfloat16, device=device)  # noqa: E731
+        self.embed = w((cfg.vocab, H), 0)
+        self.lm_head = w((cfg.vocab, H), 1)
+        self.final_norm = ones(H)
+        self.layers = []
+        for l in range(cfg.layers):
+            b = 10 + 10 * l
+            self.layers.append({
+                "in_norm": ones(H), "qkv": w((qkv_out, H), b), "q_norm": ones(D),
+                "k_norm": ones(D), "o": w((H, cfg.heads * D), b + 1), "post_norm": ones(H),
+                "gate_up": w((2 * F, H), b + 2), "down": w((H, F), b + 3)})
+
+    def host_bits(self, n_layers: int) -> dict:
+        """uint16 bit patterns of the first n_layers layers (for the oracle)."""
+        def b(t):
+            return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        out = {"embed": b(self.embed), "lm_head": b(self.lm_head),
+               "final_norm": b(self.final_norm)}
+        for l in range(n_layers):
+            for k, v in self.layers[l].items():
+                out[f"{l}.{k}"] = b(v)
+        return out
+
+
+@dataclass
+class Sequence:
+    sid: int
+    prompt: list
+    max_new: int
+    generated: list = field(default_factory=list)
+    forced: list | None = None  # teacher-forced continuation instead of argmax
+    n_cached: int = 0
+    pages: list = field(default_factory=list)
+
+    @property
+    def tokens(self):
+        return self.prompt + self.generated
+
+    @property
+    def done(self):
+        return len(self.generated) >= self.max_new
+
+
+class Engine:
+    """Paged KV cache + continuous-batching greedy decode over Qwen3Weights
+    (optionally truncated to the first n_layers layers)."""
+
+    def __init__(self, weights: Qwen3Weights, num_pages: int, max_tokens_per_step: int = 8192,
+                 n_layers: int | None = None, device="cuda"):
+        self.w = weights
+        cfg = self.cfg = weights.cfg
+        self.n_layers = n_layers or cfg.layers
+        self.device = torch.device(device)
+        self.num_pages = num_pages
+        self.budget = max_tokens_per_step
+        D, Hkv = cfg.head_dim, cfg.kv_heads
+        self.k_cache = [torch.empty(num_pages, Hkv, PAGE_SIZE, D, dtype=torch.bfloat16,
+                                    device=self.device) for _ in range(self.n_layers)]
+        self.v_cache = [torch.empty_like(k) for k in self.k_cache]
+        self.free_pages = deque(range(num_pages))
+        self.rope = rope_table(cfg.max_pos, cfg.rope_theta, D, device=self.device)
+        T, H, F = max_tokens_per_step, cfg.hidden, cfg.ffn
+        e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=self.device)  # noqa: E731
+        self.buf = {"res": e(T, H), "n": e(T, H), "qkv": e(T, (cfg.heads + 2 * Hkv) * D),
+                    "q": e(T, cfg.heads, D), "attn": e(T, cfg.heads, D), "o": e(T, H),
+                    "gu": e(T, 2 * F), "h": e(T, F), "d": e(T, H)}
+        self.steps = 0
+
+    # ------------------------------------------------------------ pages ----
+    def _ensure_pages(self, seq: Sequence, upto: int):
+        need = -(-upto // PAGE_SIZE)
+        while len(seq.pages) < need:
+            if not self.free_pages:
+                raise RuntimeError("KV cache out of pages")
+            seq.pages.append(self.free_pages.popleft())
+
+    def _release(self, seq: Sequence):
+        self.free_pages.extend(seq.pages)
+        seq.pages = []
+
+    # ---------------------------------------------------------- forward ----
+    def forward(self, items, want_logits):
+        """One step.  items: list of (seq, n) -- process the next n uncached
+        tokens of seq.  want_logits: per item, whether its last token's logits
+        are needed.  Returns logits [sum(want_logits), vocab] (bf16)."""
+        cfg = self.cfg
+        toks, pos, slots = [], [], []
+        for seq, n in items:
+            t0 = seq.n_cached
+            self._ensure_pages(seq, t0 + n)
+            all_t = seq.tokens
+            for t in range(t0, t0 + n):
+                toks.append(all_t[t])
+                pos.append(t)
+                slots.append(seq.pages[t // PAGE_SIZE] * PAGE_SIZE + t % PAGE_SIZE)
+        T = len(toks)
+        if T > self.budget:
+            raise ValueError("step exceeds the token budget")
+        dev = self.device
+        i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32)).to(dev, non_blocking=True)  # noqa: E731
+        tok_d = torch.as_tensor(np.asarray(toks, dtype=np.int64)).to(dev)
+        pos_d, slot_d = i32(pos), i32(slots)
+
+        # decode items (one token) and prompt items, each with its own metadata
+        dec = [(k, s, n) for k, (s, n) in enumerate(items) if n == 1 and s.n_cached >= len(s.prompt)]
+        pre = [(k, s, n) for k, (s, n) in enumerate(items) if not (n == 1 and s.n_cached >= len(s.prompt))]
+        offs = np.cumsum([0] + [n for _, n in items])
+
+        def table(group):
+            width = max(len(s.pages) for _, s, _ in group)
+            bt = np.full((len(group), width), -1, dtype=np.int32)
+            for r, (_, s, _) in enumerate(group):
+                bt[r, :len(s.pages)] = s.pages
+            return bt
+
+        meta = {}
+        if dec:
+            rows = np.array([offs[k] for k, _, _ in dec], dtype=np.int64)
+            lens = [s.n_cached + 1 for _, s, _ in dec]
+            bt = table(dec)
+            meta["dec"] = (torch.as_tensor(rows).to(dev), i32(bt), i32(lens), int(max(lens)),
+                           bt.shape[1])
+        if pre:
+            starts = [int(offs[k]) for k, _, _ in pre]
+            nqs = [n for _, _, n in pre]
+            # prompt rows are contiguous per item; gather them into one block
+            rows = np.concatenate([np.arange(a, a + n) for a, n in zip(starts, nqs)])
+            indptr = np.concatenate([[0], np.cumsum(nqs)])
+            lens = [s.n_cached + n for _, s, n in pre]
+            bt = table(pre)
+            meta["pre"] = (torch.as_tensor(rows).to(dev), i32(bt), i32(lens), i32(indptr),
+                           int(max(nqs)), int(max(lens)))
+
+        b = {k: v[:T] for k, v in self.buf.items()}
+        res = b["res"]
+        torch.index_select(self.w.embed, 0, tok_d, out=res)
+        Hq, Hkv = cfg.heads, cfg.kv_heads
+        for l in range(self.n_layers):
+            L = self.w.layers[l]
+            if l == 0:
+                rmsnorm(res, L["in_norm"], cfg.eps, out=b["n"])
+            else:
+                add_rmsnorm(b["d"], res, L["in_norm"], cfg.eps, out=b["n"])
+            gemm(b["n"], L["qkv"], out=b["qkv"])
+            qk_norm_rope_append(b["qkv"], Hq, Hkv, pos_d, slot_d, self.rope, L["q_norm"],
+                                L["k_norm"], self.k_cache[l], self.v_cache[l], cfg.eps,
+                                q_out=b["q"])
+            self._attention(l, b, meta)
+            gemm(b["attn"].view(T, Hq * cfg.head_dim), L["o"], out=b["o"])
+            add_rmsnorm(b["o"], res, L["post_norm"], cfg.eps, out=b["n"])
+            gemm(b["n"], L["gate_up"], out=b["gu"])
+            silu_mul(b["gu"], out=b["h"])
+            gemm(b["h"], L["down"], out=b["d"])
+        add_rmsnorm(b["d"], res, self.w.final_norm, cfg.eps, out=b["n"])
+        samp = [int(offs[k + 1] - 1) for k, want in enumerate(want_logits) if want]
+        if not samp:
+            return None
+        nrows = torch.index_select(b["n"], 0, torch.as_tensor(samp, dtype=torch.int64).to(dev))
+        self.steps += 1
+        return gemm(nrows, self.w.lm_head)
+
+    def _attention(self, l, b, meta):
+        cfg = self.cfg
+        kc, vc = self.k_cache[l], self.v_cache[l]
+        if "dec" in meta:
+            rows, bt, lens, mx, _ = meta["dec"]
+            q = torch.index_select(b["q"], 0, rows)
+            out = decode_attention(q, kc, vc, bt, lens, max_seq_len=mx)
+            b["attn"].index_copy_(0, rows, out)
+        if "pre" in meta:
+            rows, bt, lens, indptr, mq, mx = meta["pre"]
+            q = torch.index_select(b["q"], 0, rows)
+            out = prefill_attention(q, kc, vc, bt, lens, indptr, max_q_len=mq, max_seq_len=mx)
+            b["attn"].index_copy_(0, rows, out)
+
+    # ------------------------------------------------------- scheduling ----
+    def generate(self, seqs: list[Sequence], record: set | None = None):
+        """Run every sequence to max_new generated tokens.  Returns
+        {sid: [logits row per generated token]} (CPU bf16) for sids in `record`."""
+        record = record or set()
+        logs = {sid: [] for sid in record}
+        waiting = deque(seqs)
+        running: list[Sequence] = []
+        while waiting or running:
+            items, budget = [], self.budget
+            for s in running:
+                items.append((s, 1))
+                budget -= 1
+            admitted = []
+            while waiting and budget > 0:
+                s = waiting[0]
+                take = min(len(s.prompt) - s.n_cached, budget)
+                items.append((s, take))
+                budget -= take
+                if s.n_cached + take == len(s.prompt):
+                    admitted.append(waiting.popleft())
+                else:
+                    break
+            want = [s.n_cached + n == len(s.tokens) for s, n in items]
+            logits = self.forward(items, want)
+            nxt = torch.argmax(logits, dim=-1).cpu().tolist() if logits is not None else []
+            j = 0
+            for (s, n), w in zip(items, want):
+                s.n_cached += n
+                if not w:
+                    continue
+                if s.sid in record:
+                    logs[s.sid].append(logits[j].cpu())
+                tok = s.forced[len(s.generated)] if s.forced is not None else nxt[j]
+                s.generated.append(int(tok))
+                j += 1
+            running = [s for s in running + admitted if not s.done]
+            for s in seqs:
+                if s.done and s.pages:
+                    self._release(s)
+        return logs
+
+    def reset(self):
+        self.free_pages = deque(range(self.num_pages))
+        self.steps = 0
+
+
+def random_requests(n: int, vocab: int, min_len: int, max_len: int, max_new: int,
+                    seed: int = 7) -> list[Sequence]:
+    """n requests with prompt lengths uniform on [min_len, max_len] and token
+    ids uniform on [0, vocab)."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(min_len, max_len + 1, (n,), generator=g).tolist()
+    out = []
+    for i, L in enumerate(lens):
+        prompt = torch.randint(0, vocab, (L,), generator=g).tolist()
+        out.append(Sequence(sid=i, prompt=prompt, max_new=max_new))
+    return out

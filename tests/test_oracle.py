@@ -343,3 +343,62 @@ def test_attention_rejects_empty_sequence():
     p["seq_lens"] = torch.tensor([4, 0], dtype=torch.int32)
     with pytest.raises(ValueError):
         oracle.decode_attention(**p)
+
+
+# ---------------------------------------------------- decoder primitives ----
+from oracle import decoder as odec  # noqa: E402
+
+
+def test_rope_position_zero_is_identity_and_norms_are_kept():
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((3, 5, 128))
+    np.testing.assert_array_equal(odec.rope(x, np.zeros(5), 1e6), x)
+    y = odec.rope(x, np.arange(5) * 37, 1e6)
+    # each (i, 64 + i) pair is rotated, so its length is kept
+    np.testing.assert_allclose(np.hypot(y[..., :64], y[..., 64:]),
+                               np.hypot(x[..., :64], x[..., 64:]), rtol=1e-13)
+
+
+def test_rope_closed_form_and_composition():
+    x = np.zeros((1, 1, 128))
+    x[0, 0, 0], x[0, 0, 64] = 2.0, -3.0  # pair i = 0 has frequency theta^0 = 1
+    y = odec.rope(x, np.array([1]), 1e6)[0, 0]
+    assert y[0] == pytest.approx(2.0 * math.cos(1.0) + 3.0 * math.sin(1.0), rel=1e-15)
+    assert y[64] == pytest.approx(-3.0 * math.cos(1.0) + 2.0 * math.sin(1.0), rel=1e-15)
+    # pair i = 32 has frequency theta^(-1/2) = 1e-3 at theta = 1e6
+    x = np.zeros((1, 1, 128))
+    x[0, 0, 32] = 1.0
+    y = odec.rope(x, np.array([500]), 1e6)[0, 0]
+    assert y[32] == pytest.approx(math.cos(0.5), rel=1e-13)
+    assert y[96] == pytest.approx(math.sin(0.5), rel=1e-13)
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal((1, 1, 128))
+    a = odec.rope(odec.rope(z, np.array([70]), 1e4), np.array([30]), 1e4)
+    np.testing.assert_allclose(a, odec.rope(z, np.array([100]), 1e4), rtol=1e-11, atol=1e-13)
+
+
+def test_silu_closed_forms():
+    g = np.array([0.0, 1.0, -1.0, 40.0, -40.0])
+    u = np.ones_like(g)
+    s = odec.silu_mul(g, u)
+    assert s[0] == 0.0
+    assert s[1] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    assert s[2] == pytest.approx(-1.0 / (1.0 + math.e), rel=1e-15)
+    assert s[3] == pytest.approx(40.0, rel=1e-15) and abs(s[4]) < 1e-15
+    assert odec.silu_mul(np.array([2.0]), np.array([3.0]))[0] == pytest.approx(6.0 / (1 + math.exp(-2)))
+
+
+def test_causal_attention_first_row_and_equal_keys():
+    rng = np.random.default_rng(12)
+    T, Hq, Hkv, D = 6, 8, 2, 128
+    q = rng.standard_normal((T, Hq, D))
+    k = rng.standard_normal((T, Hkv, D))
+    v = rng.standard_normal((T, Hkv, D))
+    o = odec.causal_attention(q, k, v, 1 / math.sqrt(D))
+    for i in range(Hq):  # position 0 sees one key: its value
+        np.testing.assert_allclose(o[0, i], v[0, i // 4], rtol=1e-15)
+    k[:] = k[0]  # equal keys: every row averages the values it can see
+    o = odec.causal_attention(q, k, v, 1 / math.sqrt(D))
+    for t in range(T):
+        for i in range(Hq):
+            np.testing.assert_allclose(o[t, i], v[:t + 1, i // 4].mean(axis=0), rtol=1e-12)
