@@ -6,9 +6,13 @@
 // tokens (rows of K and V) and 8 columns (query head x query row pairs):
 //     S^T[16 x 8] = K_page[16 x 128] . Q^T[128 x 8]       8 mma.sync, dims ascending
 //     x = S * scale * log2(e)        (tokens past a column's length -> -inf)
-//     m' = max(m, max_t x);  alpha = 2^(m - m');  p = bf16(2^(x - m'))
+//     m' = max(m, max_t x);  alpha = 2^(m - m');  p = 2^(x - m')  (fp32)
 //     l' = l * alpha + sum_t p       (fixed xor-butterfly order over tokens)
-//     O^T[128 x 8] = O^T * alpha + V^T[128 x 16] . P^T[16 x 8]   8 mma.sync
+//     p = p_hi + p_lo with p_hi = bf16(p), p_lo = bf16(p - p_hi)
+//     O^T[128 x 8] = (O^T * alpha + V^T . P_hi^T) + V^T . P_lo^T   16 mma.sync
+// Splitting p keeps the weights to about 16 significant bits in the PV
+// product (one bf16 operand alone would keep 8), at the price of a second
+// mma per 16 dims -- cheap in a kernel bound by HBM.
 // Each output element of an mma depends only on its own column, so a column's
 // result does not depend on what shares the tile with it.
 //
@@ -99,11 +103,14 @@ __device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint
     const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mn1);
     const float p2 = x2 == -INFINITY ? 0.f : exp2f(x2 - mn0);
     const float p3 = x3 == -INFINITY ? 0.f : exp2f(x3 - mn1);
-    const uint32_t pA = bi::pack_bf16x2(p0, p1);
+    const uint32_t pA = bi::pack_bf16x2(p0, p1);  // high parts
     const uint32_t pB = bi::pack_bf16x2(p2, p3);
-    // the sums use the same bf16-rounded weights that multiply V
-    float ps0 = __uint_as_float(pA << 16) + __uint_as_float(pB << 16);
-    float ps1 = __uint_as_float(pA & 0xffff0000u) + __uint_as_float(pB & 0xffff0000u);
+    const uint32_t rA = bi::pack_bf16x2(__fsub_rn(p0, __uint_as_float(pA << 16)),
+                                        __fsub_rn(p1, __uint_as_float(pA & 0xffff0000u)));
+    const uint32_t rB = bi::pack_bf16x2(__fsub_rn(p2, __uint_as_float(pB << 16)),
+                                        __fsub_rn(p3, __uint_as_float(pB & 0xffff0000u)));
+    float ps0 = __fadd_rn(p0, p2);
+    float ps1 = __fadd_rn(p1, p3);
 #pragma unroll
     for (int off = 4; off <= 16; off <<= 1) {
         ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
@@ -123,11 +130,14 @@ __device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint
     // P^T fragments (tokens on K, columns on N) by an in-register transpose
     const uint32_t pb0 = bi::movmatrix_trans(pA);
     const uint32_t pb1 = bi::movmatrix_trans(pB);
+    const uint32_t lb0 = bi::movmatrix_trans(rA);
+    const uint32_t lb1 = bi::movmatrix_trans(rB);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         uint32_t a0, a1, a2, a3;
         bi::ldmatrix_x4_trans(vs_base + swz(lm_r + 8 * (lm_j >> 1), 2 * mt + (lm_j & 1)), a0, a1, a2, a3);
         bi::mma_bf16_16816(st.acc[mt], a0, a1, a2, a3, pb0, pb1);
+        bi::mma_bf16_16816(st.acc[mt], a0, a1, a2, a3, lb0, lb1);
     }
 }
 
