@@ -65,8 +65,14 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "attention", "rmsnorm"],
+    ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "attention", "rmsnorm",
+                                       "decoder"],
                     help="time one kernel of the path alone (for profiling); prints its own line")
+    ap.add_argument("--requests", type=int, default=1000, help="--case decoder: requests")
+    ap.add_argument("--layers", type=int, default=36, help="--case decoder: decoder layers")
+    ap.add_argument("--new-tokens", type=int, default=100, help="--case decoder: tokens per request")
+    ap.add_argument("--track", type=int, default=16,
+                    help="--case decoder: requests re-run alone for the bitwise check")
     ap.add_argument("--batch", type=int, default=ATT_B,
                     help="sequences for --case attention (a smaller case for ncu captures)")
     return ap.parse_args()
@@ -595,9 +601,72 @@ def run_case(args):
                       "value": round(work / (ms * 1e-3) / scale, 2), "unit": unit}), flush=True)
 
 
+def run_decoder(args):
+    """The random-init Qwen3-8B-shaped decoder served with continuous batching:
+    `requests` prompts of U[32, 512] random tokens, `new_tokens` greedy tokens
+    each, at most 8192 tokens per step (prompts split across steps as needed).
+    Timed: the whole batched run (wall clock, host scheduling included).  Then
+    `track` requests are re-run alone and their logits compared bit for bit
+    with the batched run at every generated token; the same batched run with
+    torch/cuBLAS GEMMs and torch RMSNorms swapped in is timed and checked the
+    same way, as the non-invariant comparison."""
+    import __graft_entry__
+    from invariant_bi_rmsnorm_gb300 import qwen3
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    cfg = qwen3.Qwen3Config(layers=args.layers)
+    w = qwen3.Qwen3Weights(cfg, seed=1000)
+    budget = 8192
+
+    def requests():
+        return qwen3.random_requests(args.requests, cfg.vocab, 32, 512, args.new_tokens, seed=7)
+
+    reqs = requests()
+    pages = sum(-(-(len(r.prompt) + args.new_tokens) // 16) for r in reqs) + 64
+    track = sorted({int(i) for i in np.linspace(0, args.requests - 1, args.track)})
+    result = {"case": "decoder", "requests": args.requests, "layers": args.layers,
+              "prompt_len": "U[32,512]", "new_tokens": args.new_tokens,
+              "max_tokens_per_step": budget, "model": "random-init Qwen3-8B-shaped "
+              "(hidden 4096, FFN 12288, 32/8 heads, d128, vocab 151936, RoPE 1e6)",
+              "prompt_tokens": int(sum(len(r.prompt) for r in reqs))}
+    for ops in ("bi", "torch"):
+        eng = qwen3.Engine(w, num_pages=pages, max_tokens_per_step=budget, ops=ops)
+        warm = qwen3.random_requests(4, cfg.vocab, 32, 64, 2, seed=99)
+        eng.generate(warm)
+        eng.reset()
+        reqs = requests()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        logs = eng.generate(reqs, record=set(track))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        steps = eng.steps
+        mism_logits = mism_tokens = 0
+        for sid in track:
+            eng.reset()
+            one = qwen3.Sequence(sid=sid, prompt=list(reqs[sid].prompt), max_new=args.new_tokens)
+            alone = eng.generate([one], record={sid})
+            mism_tokens += int(one.generated != reqs[sid].generated)
+            mism_logits += sum(int(not torch.equal(a, b)) for a, b in zip(alone[sid], logs[sid]))
+        toks = result["prompt_tokens"] + args.requests * args.new_tokens
+        result[ops] = {"wall_s": round(wall, 3), "steps": steps,
+                       "tokens_per_s": round(toks / wall, 1),
+                       "tracked_requests": len(track),
+                       "logit_rows_compared": len(track) * args.new_tokens,
+                       "logit_rows_differing_alone_vs_batched": mism_logits,
+                       "requests_whose_tokens_differ": mism_tokens}
+        del eng
+        torch.cuda.empty_cache()
+    result["bitwise_invariant"] = result["bi"]["logit_rows_differing_alone_vs_batched"] == 0
+    result["cost_vs_torch_ops"] = round(result["bi"]["wall_s"] / result["torch"]["wall_s"], 4)
+    print(json.dumps(result), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.case:
+    if args.case == "decoder":
+        run_decoder(args)
+    elif args.case:
         run_case(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -103,7 +103,13 @@ class Engine:
     (optionally truncated to the first n_layers layers)."""
 
     def __init__(self, weights: Qwen3Weights, num_pages: int, max_tokens_per_step: int = 8192,
-                 n_layers: int | None = None, device="cuda"):
+                 n_layers: int | None = None, device="cuda", ops: str = "bi"):
+        """ops="bi": every GEMM and RMSNorm through this library (batch-invariant).
+        ops="torch": GEMMs through torch.matmul (cuBLAS) and RMSNorms through
+        torch.nn.functional.rms_norm instead -- the non-invariant comparison."""
+        if ops not in ("bi", "torch"):
+            raise ValueError("ops must be 'bi' or 'torch'")
+        self.ops = ops
         self.w = weights
         cfg = self.cfg = weights.cfg
         self.n_layers = n_layers or cfg.layers
@@ -190,6 +196,7 @@ class Engine:
 
         b = {k: v[:T] for k, v in self.buf.items()}
         res = b["res"]
+        gemm, rmsnorm, add_rmsnorm = self._ops()
         torch.index_select(self.w.embed, 0, tok_d, out=res)
         Hq, Hkv = cfg.heads, cfg.kv_heads
         for l in range(self.n_layers):
@@ -214,7 +221,26 @@ class Engine:
             return None
         nrows = torch.index_select(b["n"], 0, torch.as_tensor(samp, dtype=torch.int64).to(dev))
         self.steps += 1
-        return gemm(nrows, self.w.lm_head)
+        return gemm(nrows, self.w.lm_head, out=torch.empty(len(samp), cfg.vocab,
+                                                           dtype=torch.bfloat16, device=dev))
+
+    def _ops(self):
+        if self.ops == "bi":
+            return gemm, rmsnorm, add_rmsnorm
+        import torch.nn.functional as F
+
+        def t_gemm(x, W, out=None):
+            return torch.matmul(x, W.t(), out=out)
+
+        def t_rmsnorm(x, w, eps, out=None):
+            out.copy_(F.rms_norm(x, (x.shape[-1],), w, eps))
+            return out
+
+        def t_add_rmsnorm(x, res, w, eps, out=None):
+            res.add_(x)
+            out.copy_(F.rms_norm(res, (res.shape[-1],), w, eps))
+            return out
+        return t_gemm, t_rmsnorm, t_add_rmsnorm
 
     def _attention(self, l, b, meta):
         cfg = self.cfg
