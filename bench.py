@@ -65,8 +65,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "attention", "rmsnorm",
-                                       "decoder"],
+    ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "gemm_layers", "attention",
+                                       "rmsnorm", "decoder"],
                     help="time one kernel of the path alone (for profiling); prints its own line")
     ap.add_argument("--requests", type=int, default=1000, help="--case decoder: requests")
     ap.add_argument("--layers", type=int, default=36, help="--case decoder: decoder layers")
@@ -195,7 +195,8 @@ class Workload:
         self.att_bytes = float((lens * HKV * HD * 2 * 2).sum() + ATT_B * HQ * HD * 2 * 2
                                + 4 * pages.sum() + 4 * ATT_B)
         self.att_flops = float((4.0 * HQ * HD * lens).sum())
-        self.launches_per_step = 1 + len(LAYERS) + 2
+        self.launches_per_step = 1 + len(LAYERS) + int(
+            bi._lib.load().bi_decode_attention_launches(ATT_B, HKV, MAX_LEN))
         torch.cuda.synchronize(dev)
 
     def rmsnorm(self):
@@ -562,7 +563,17 @@ def run_case(args):
     __graft_entry__.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.case.startswith("gemm"):
+    if args.case == "gemm_layers":
+        # the bench step's four GEMM launches (qkv, o, gate_up, down at M = 4096)
+        xs = {K: inputs.gemm_rows(GEMM_M, K, seed=50 + K, device=dev) for _, _, K in LAYERS}
+        Ws = [inputs.gemm_weight(N, K, seed=40 + i, device=dev) for i, (_, N, K) in enumerate(LAYERS)]
+        ys = [torch.empty(GEMM_M, N, dtype=torch.bfloat16, device=dev) for _, N, _ in LAYERS]
+
+        def fn():
+            for (_, N, K), W, y in zip(LAYERS, Ws, ys):
+                bi.gemm(xs[K], W, out=y)
+        work, unit = sum(2.0 * GEMM_M * N * K for _, N, K in LAYERS), "TFLOP/s"
+    elif args.case.startswith("gemm"):
         n, N, K = {"gemm_gate_up": LAYERS[2], "gemm_qkv": LAYERS[0]}[args.case]
         x = inputs.gemm_rows(GEMM_M, K, seed=50 + K, device=dev)
         W = inputs.gemm_weight(N, K, seed=42, device=dev)

@@ -300,6 +300,12 @@ bi_status bi_decode_attention_fixed_splits(const void* q, const void* k_cache,
                                            void* out, void* workspace, size_t workspace_bytes,
                                            cudaStream_t stream);
 
+/* Kernel launches one bi_decode_attention call makes on the current device:
+ * 1 when every sequence's chunks are folded inside its CTA, 2 when the merge
+ * kernel runs too.  A schedule detail -- the results are the same bits either
+ * way.  0 for invalid arguments or when no device is available. */
+int32_t bi_decode_attention_launches(int32_t B, int32_t Hkv, int32_t max_seq_len);
+
 /*
  * bi_decode_attention_noalloc -- bi_decode_attention for callers that cannot
  * allocate device memory when they call it.

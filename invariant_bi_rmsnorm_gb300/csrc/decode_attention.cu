@@ -352,6 +352,16 @@ extern "C" int32_t bi_decode_chunk_len(int32_t seq_len, int32_t c) {
 
 namespace {
 
+// Schedule (never the arithmetic): how many consecutive chunks one CTA
+// walks -- enough CTAs for about four waves of the resident slots (3 CTAs per
+// SM), between 4 (one per warp) and 32.
+int chunks_per_cta(int64_t B, int64_t Hkv, int64_t max_chunks, int sms) {
+    const int64_t slots = static_cast<int64_t>(sms) * 3;
+    const int64_t units = B * Hkv * max_chunks;
+    return static_cast<int>(
+        std::min<int64_t>(kMaxChunksPerCta, std::max<int64_t>(kWarps, units / (4 * slots))));
+}
+
 // Validate and launch split + merge.  num_splits == 0 is the batch-invariant
 // fixed split size; num_splits > 0 the fixed-split-count comparison variant,
 // whose workspace then holds num_splits partials per (sequence, query head).
@@ -424,16 +434,11 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     args.num_splits = num_splits;
     args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
-    // Schedule (never the arithmetic): how many consecutive chunks one CTA
-    // walks.  Enough CTAs for about four waves of the resident slots; a
-    // sequence whose chunks all fall to one CTA is folded there, the rest by
+    // A sequence whose chunks all fall to one CTA is folded there, the rest by
     // the merge kernel -- both apply the same fold in the same chunk order.
     int cpc = 1;
     if (num_splits == 0) {
-        const int64_t slots = static_cast<int64_t>(bi::sm_count()) * 3;  // 3 CTAs per SM
-        const int64_t units = static_cast<int64_t>(B) * Hkv * max_chunks;
-        cpc = static_cast<int>(std::min<int64_t>(kMaxChunksPerCta,
-                                                 std::max<int64_t>(kWarps, units / (4 * slots))));
+        cpc = chunks_per_cta(B, Hkv, max_chunks, bi::sm_count());
     } else {
         // comparison variant: up to one split per warp, within the page list
         const int ppc_max = ceil_div(ceil_div(max_seq_len, kPage), num_splits);
@@ -454,6 +459,14 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
 }
 
 }  // namespace
+
+extern "C" int32_t bi_decode_attention_launches(int32_t B, int32_t Hkv, int32_t max_seq_len) {
+    if (B < 1 || Hkv < 1 || max_seq_len < 1) return 0;
+    const int sms = bi::sm_count();
+    if (sms <= 0) return 0;
+    const int max_chunks = ceil_div(max_seq_len, kChunk);
+    return max_chunks > chunks_per_cta(B, Hkv, max_chunks, sms) ? 2 : 1;
+}
 
 extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                                          const int32_t* block_table, int32_t max_pages_per_seq,
