@@ -277,6 +277,27 @@ bi_status bi_silu_mul(const void* gate_up, int64_t ld_gate_up, int32_t T, int32_
                       int64_t ld_out, cudaStream_t stream);
 
 /*
+ * bi_logprobs -- per-row log-sum-exp of bf16 logits and the log-probability
+ * of one target token per row:
+ *     lse[r] = log sum_j exp(x[r][j]),   logprob[r] = x[r][targets[r]] - lse[r]   (fp32)
+ *
+ * Operation: the sampler/trainer agreement that "Defeating Nondeterminism in
+ * LLM Inference: The Core Role of Batch Invariance" ("Experimental Validation
+ * and Future Prospects", true on-policy RL) needs: the softmax denominator is
+ * a reduction over the vocabulary, computed one row per CTA in an order that
+ * depends only on `vocab` (max, then sum of exp(x - max) over fixed per-thread
+ * strides, a warp butterfly and a warp-ordered fold), so a row's results are
+ * bit-identical in any batch.
+ *   logits   device, bf16 [rows][ld], ld >= vocab, both multiples of 8.
+ *   targets  device, int32 [rows] or null;  logprob_out  device, fp32 [rows]
+ *            (needed with targets);  lse_out  device, fp32 [rows] or null.
+ * A target outside 0 .. vocab-1 gives NaN and BI_ERR_DEVICE_BAD_INPUT.
+ */
+bi_status bi_logprobs(const void* logits, int64_t rows, int32_t vocab, int64_t ld,
+                      const int32_t* targets, float* logprob_out, float* lse_out,
+                      cudaStream_t stream);
+
+/*
  * bi_decode_attention_fixed_splits -- the same attention with a fixed split
  * COUNT instead of a fixed split size: each sequence's pages are cut into
  * num_splits nearly equal runs (ceil(ceil(L/16)/num_splits) pages each), so

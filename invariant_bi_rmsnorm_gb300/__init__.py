@@ -25,7 +25,7 @@ from ._lib import DECODE_CHUNK, PAGE_SIZE
 
 __all__ = ["BiError", "rmsnorm", "gemm", "decode_attention", "decode_attention_fixed_splits",
            "prefill_attention", "add_rmsnorm", "qk_norm_rope_append", "silu_mul",
-           "rope_table",
+           "rope_table", "logprobs",
            "decode_attention_workspace_size", "selftest_wait_timeout",
            "decode_num_chunks", "decode_chunk_len", "get_device_error", "abi_version",
            "status_string", "PAGE_SIZE", "DECODE_CHUNK"]
@@ -174,6 +174,24 @@ def silu_mul(gate_up: torch.Tensor, out: torch.Tensor | None = None, stream=None
                                    out.data_ptr(), _row_major_2d(out, "out"), _stream(stream)),
            "bi_silu_mul")
     return out
+
+
+def logprobs(logits: torch.Tensor, targets: torch.Tensor | None = None, stream=None):
+    """(logprob of targets [rows] fp32 or None, lse [rows] fp32) of bf16 logits
+    [rows, vocab], batch-invariant per row."""
+    _cuda_bf16(logits, "logits")
+    rows, vocab = logits.shape
+    lse = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    lp = None
+    if targets is not None:
+        if not targets.is_cuda or targets.dtype != torch.int32 or not targets.is_contiguous():
+            raise ValueError("targets must be a contiguous int32 CUDA tensor")
+        lp = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    _check(_lib.load().bi_logprobs(logits.data_ptr(), rows, vocab, _row_major_2d(logits, "logits"),
+                                   targets.data_ptr() if targets is not None else None,
+                                   lp.data_ptr() if lp is not None else None, lse.data_ptr(),
+                                   _stream(stream)), "bi_logprobs")
+    return lp, lse
 
 
 # ---------------------------------------------------------------- GEMM ------

@@ -29,7 +29,7 @@ EXPORTS = (
     "bi_decode_attention_workspace_size", "bi_decode_num_chunks", "bi_decode_chunk_len",
     "bi_decode_attention", "bi_decode_attention_noalloc", "bi_decode_attention_fixed_splits",
     "bi_selftest_wait_timeout", "bi_prefill_attention", "bi_add_rmsnorm",
-    "bi_qk_norm_rope_append", "bi_silu_mul", "bi_decode_attention_launches",
+    "bi_qk_norm_rope_append", "bi_silu_mul", "bi_decode_attention_launches", "bi_logprobs",
 )
 
 _lib = None
@@ -91,6 +91,8 @@ def load() -> ctypes.CDLL:
     lib.bi_silu_mul.restype = ctypes.c_int
     lib.bi_decode_attention_launches.argtypes = [_i32, _i32, _i32]
     lib.bi_decode_attention_launches.restype = _i32
+    lib.bi_logprobs.argtypes = [_vp, _i64, _i32, _i64, _vp, _vp, _vp, _vp]
+    lib.bi_logprobs.restype = ctypes.c_int
     lib.bi_selftest_wait_timeout.argtypes = [_i32, _vp]
     lib.bi_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib

@@ -23,7 +23,7 @@ LIB = os.path.join(PKG, "libbi.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 
 SOURCES = ["api.cu", "rmsnorm.cu", "gemm.cu", "decode_attention.cu", "prefill_attention.cu",
-           "decoder_ops.cu"]
+           "decoder_ops.cu", "logprobs.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

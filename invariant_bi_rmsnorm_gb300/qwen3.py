@@ -25,8 +25,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import (add_rmsnorm, decode_attention, decode_attention_workspace_size, gemm,
-               prefill_attention, qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
+from . import (add_rmsnorm, decode_attention, gemm, logprobs, prefill_attention,
+               qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
 from . import inputs
 from ._lib import PAGE_SIZE
 
@@ -259,9 +259,12 @@ class Engine:
     # ------------------------------------------------------- scheduling ----
     def generate(self, seqs: list[Sequence], record: set | None = None):
         """Run every sequence to max_new generated tokens.  Returns
-        {sid: [logits row per generated token]} (CPU bf16) for sids in `record`."""
+        {sid: [logits row per generated token]} (CPU bf16) for sids in `record`;
+        the log-probability of each generated token (bi_logprobs, fp32) goes to
+        self.logprobs[sid] for the same sids."""
         record = record or set()
         logs = {sid: [] for sid in record}
+        self.logprobs = {sid: [] for sid in record}
         waiting = deque(seqs)
         running: list[Sequence] = []
         while waiting or running:
@@ -281,7 +284,16 @@ class Engine:
                     break
             want = [s.n_cached + n == len(s.tokens) for s, n in items]
             logits = self.forward(items, want)
-            nxt = torch.argmax(logits, dim=-1).cpu().tolist() if logits is not None else []
+            chosen = []
+            if logits is not None:
+                nxt = torch.argmax(logits, dim=-1).cpu().tolist()
+                sampled = [s for (s, n), w in zip(items, want) if w]
+                chosen = [s.forced[len(s.generated)] if s.forced is not None else nxt[j]
+                          for j, s in enumerate(sampled)]
+                if record:
+                    tgt = torch.as_tensor(np.asarray(chosen, dtype=np.int32)).to(self.device)
+                    lps, _ = logprobs(logits, tgt)
+                    lps = lps.cpu()
             j = 0
             for (s, n), w in zip(items, want):
                 s.n_cached += n
@@ -289,8 +301,8 @@ class Engine:
                     continue
                 if s.sid in record:
                     logs[s.sid].append(logits[j].cpu())
-                tok = s.forced[len(s.generated)] if s.forced is not None else nxt[j]
-                s.generated.append(int(tok))
+                    self.logprobs[s.sid].append(lps[j].clone())
+                s.generated.append(int(chosen[j]))
                 j += 1
             running = [s for s in running + admitted if not s.done]
             for s in seqs:

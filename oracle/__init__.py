@@ -25,6 +25,8 @@ Pins (checked by ``tests/test_oracle.py`` without reference to this code):
                         scipy-softmax evaluation of gathered pages
   decode_attention_chunked ... equals the unchunked definition; chunk plan
                         1000 -> 256, 256, 256, 232 from the pages
+  logprobs ............ uniform row (-log V), two-level row closed form,
+                        scipy logsumexp, probabilities summing to 1
 No function is left "parity unpinned".
 """
 from __future__ import annotations
@@ -72,6 +74,8 @@ def _load():
     lib.oracle_decode_attention_chunked.argtypes = attn_common + [
         ctypes.c_int32, ctypes.c_int32, _f64p, _f64p]
     lib.oracle_decode_attention_chunked.restype = ctypes.c_int
+    lib.oracle_logprobs.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int32, _i32p, _f64p, _f64p]
+    lib.oracle_logprobs.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -217,3 +221,18 @@ def decode_attention_chunked(q, k_cache, v_cache, block_table, seq_lens,
     if rc != 0:
         raise ValueError(f"oracle_decode_attention_chunked failed ({rc})")
     return (out, part) if want_partials else out
+
+
+def logprobs(logits, targets=None):
+    """(logprob of targets [rows], lse [rows]) of bf16 logits [rows, vocab], fp64."""
+    lb = _bits(logits)
+    rows, vocab = lb.shape
+    lse = np.empty(rows, dtype=np.float64)
+    lp = np.empty(rows, dtype=np.float64)
+    t = _i32(targets).ravel() if targets is not None else None
+    rc = _load().oracle_logprobs(_p(lb, _u16p), rows, vocab,
+                                 _p(t, _i32p) if t is not None else None,
+                                 _p(lp, _f64p) if t is not None else None, _p(lse, _f64p))
+    if rc != 0:
+        raise ValueError(f"oracle_logprobs failed ({rc})")
+    return (lp if t is not None else None), lse

@@ -319,3 +319,37 @@ int oracle_decode_attention_chunked(
     }
     return bad ? -2 : 0;
 }
+
+/* ---- log-probabilities ---------------------------------------------------
+ * "Experimental Validation and Future Prospects" (true on-policy RL): the
+ * log-probability of a token under the softmax of a logits row,
+ *     lse = log sum_j exp(x_j),   logprob(t) = x_t - lse,
+ * evaluated as m + log(sum_j exp(x_j - m)) with m = max_j x_j. */
+int oracle_logprobs(const uint16_t* logits, int64_t rows, int32_t vocab,
+                    const int32_t* targets, double* logprob, double* lse) {
+    if (rows < 0 || vocab <= 0) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* x = logits + r * (int64_t)vocab;
+        double m = -INFINITY;
+        for (int32_t j = 0; j < vocab; ++j) {
+            double v = bf16_to_double(x[j]);
+            if (v > m) m = v;
+        }
+        double s = 0.0;
+        for (int32_t j = 0; j < vocab; ++j) s += exp(bf16_to_double(x[j]) - m);
+        double l = m + log(s);
+        if (lse) lse[r] = l;
+        if (targets && logprob) {
+            int32_t t = targets[r];
+            if (t < 0 || t >= vocab) {
+                logprob[r] = NAN;
+                bad = 1;
+            } else {
+                logprob[r] = bf16_to_double(x[t]) - l;
+            }
+        }
+    }
+    return bad ? -2 : 0;
+}

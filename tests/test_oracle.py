@@ -402,3 +402,32 @@ def test_causal_attention_first_row_and_equal_keys():
     for t in range(T):
         for i in range(Hq):
             np.testing.assert_allclose(o[t, i], v[:t + 1, i // 4].mean(axis=0), rtol=1e-12)
+
+
+# ------------------------------------------------------- log-probabilities ----
+def test_logprobs_uniform_row_is_minus_log_vocab():
+    V = 4096
+    x = torch.full((2, V), 1.5, dtype=torch.bfloat16)
+    lp, lse = oracle.logprobs(x, np.array([0, 777]))
+    np.testing.assert_allclose(lp, -math.log(V), rtol=1e-14)
+    np.testing.assert_allclose(lse, 1.5 + math.log(V), rtol=1e-14)
+
+
+def test_logprobs_two_level_row_closed_form():
+    V, a, b = 1000, 6.0, -2.0
+    x = torch.full((1, V), b, dtype=torch.bfloat16)
+    x[0, 3] = a
+    lp, lse = oracle.logprobs(x, np.array([3]))
+    want = math.log(math.exp(a) + (V - 1) * math.exp(b))
+    assert lse[0] == pytest.approx(want, rel=1e-14)
+    assert lp[0] == pytest.approx(a - want, rel=1e-13)
+
+
+def test_logprobs_against_scipy_and_normalisation():
+    from scipy.special import logsumexp
+    x = inputs.normal_bf16((3, 2048), seed=90, std=3.0)
+    xs = x.double().numpy()
+    _, lse = oracle.logprobs(x)
+    np.testing.assert_allclose(lse, logsumexp(xs, axis=1), rtol=1e-13)
+    lps = np.stack([oracle.logprobs(x, np.full(3, j))[0] for j in range(0, 2048, 1)], axis=1)
+    np.testing.assert_allclose(np.exp(lps).sum(axis=1), 1.0, rtol=1e-12)

@@ -51,12 +51,16 @@ def test_logits_bit_identical_alone_and_batched(two_layer):
     track = {0, 5, 13, 23}
     eng = qwen3.Engine(w, num_pages=24 * 12, max_tokens_per_step=300)
     batched = eng.generate(reqs, record=track)
+    batched_lp = dict(eng.logprobs)
     assert eng.steps > 10  # prompts were split and mixed over many steps
     for sid in sorted(track):
         r = reqs[sid]
         eng.reset()
         alone_req = qwen3.Sequence(sid=sid, prompt=list(r.prompt), max_new=6)
+        lp_batched = list(batched_lp[sid])
         alone = eng.generate([alone_req], record={sid})
         assert alone_req.generated == r.generated, f"sequence {sid}: tokens differ"
         for step, (a, b) in enumerate(zip(alone[sid], batched[sid])):
             assert np.array_equal(bits(a), bits(b)), f"sequence {sid}: logits differ at step {step}"
+        # the sampler's log-probabilities of its own tokens agree bit for bit too
+        assert all(torch.equal(a, b) for a, b in zip(eng.logprobs[sid], lp_batched))
