@@ -161,6 +161,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------- multi-rank -----
+def reduce_max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of `values` over all ranks (each rank's timings; the
+    slowest rank sets the job time).  Identity without a process group."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def weak_scaling_rate(units_per_rank: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processed the same per-rank work."""
+    return world * units_per_rank * steps / (max_ms * 1e-3)
+
+
 # ------------------------------------------------------------ our arm -------
 class Workload:
     def __init__(self, dev):
@@ -330,14 +345,12 @@ def run_ours(args):
     rms_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
     gemm_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
     att_ms = sum(e[2].elapsed_time(e[3]) for e in evs)
-    times = torch.tensor([total_ms, rms_ms, gemm_ms, att_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, rms_ms, gemm_ms, att_ms = times.tolist()
+    total_ms, rms_ms, gemm_ms, att_ms = reduce_max_over_ranks(
+        [total_ms, rms_ms, gemm_ms, att_ms], dist, device=dev)
     K = args.steps
-    gemm_tflops = world * wl.gemm_flops * K / (gemm_ms * 1e-3) / 1e12
-    att_gbs = world * wl.att_bytes * K / (att_ms * 1e-3) / 1e9
-    rms_gbs = world * wl.rms_bytes * K / (rms_ms * 1e-3) / 1e9
+    gemm_tflops = weak_scaling_rate(wl.gemm_flops, world, K, gemm_ms) / 1e12
+    att_gbs = weak_scaling_rate(wl.att_bytes, world, K, att_ms) / 1e9
+    rms_gbs = weak_scaling_rate(wl.rms_bytes, world, K, rms_ms) / 1e9
     per_gpu_gemm = gemm_tflops / world
 
     e2e = None
@@ -445,11 +458,8 @@ def run_e2e(wl, args, dev, barrier, dist, world):
         e2e_step()
     e1.record(wl.stream)
     barrier()
-    ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    ms = ms.item()
-    return {"value": round(world * wl.gemm_flops * args.steps / (ms * 1e-3) / 1e12, 2),
+    ms = reduce_max_over_ranks([e0.elapsed_time(e1)], dist, device=dev)[0]
+    return {"value": round(weak_scaling_rate(wl.gemm_flops, world, args.steps, ms) / 1e12, 2),
             "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / args.steps, 4),
             "what": ("GEMM FLOPs of one step / wall time of the whole step through the Python API: "

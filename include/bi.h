@@ -122,7 +122,7 @@ bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y, 
  *   x  device, bf16 [M][ld_x] row-major (K contiguous).
  *   W  device, bf16 [N][ld_w] row-major: the nn.Linear weight layout.
  *   y  device, bf16 [M][ld_y] row-major; must not overlap x or W.
- *   M  0 .. 2^31-1;  N, K  >= 8 and multiples of 8.
+ *   M  0 .. 2^31-129;  N, K  >= 8 and multiples of 8.
  *   ld_x, ld_w, ld_y  in elements, multiples of 8, >= K, >= K, >= N.
  * Pointers must be 16-byte aligned.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
  * MISALIGNED, CUDA.

@@ -227,6 +227,7 @@ extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, i
                              int32_t K, int64_t ld_x, int64_t ld_w, int64_t ld_y,
                              cudaStream_t stream) {
     if (M < 0 || N < 8 || K < 8) return M < 0 ? BI_ERR_INVALID_ARG : BI_ERR_UNSUPPORTED_SHAPE;
+    if (M > 0x7fffffff - BM) return BI_ERR_UNSUPPORTED_SHAPE;  // row indices stay in int
     if ((N & 7) || (K & 7)) return BI_ERR_UNSUPPORTED_SHAPE;
     if (ld_x < K || ld_w < K || ld_y < N) return BI_ERR_INVALID_ARG;
     if ((ld_x & 7) || (ld_w & 7) || (ld_y & 7)) return BI_ERR_MISALIGNED;
