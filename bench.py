@@ -287,6 +287,29 @@ class Workload:
         t = timeit(cublas)
         res["cublas_tflops"] = self.gemm_flops / (t * 1e-3) / 1e12
         res["cublas_ms"] = t
+        # bi_gemm over the C3 batch sizes: tensor roofline at large M, weight
+        # streaming (HBM) at small M; cuBLAS on the same shapes beside it
+        by_m = {}
+        hbm = load_peaks()[0]
+        for M in (1, 8, 64, 256, 1024, 4096):
+            xs = {K: self.gx[K][:M] for K in self.gx}
+            outs = {n: self.gy[n][:M] for n in self.gy}
+
+            def ours():
+                for n, N, K in LAYERS:
+                    self.bi.gemm(xs[K], self.W[n], out=outs[n])
+
+            def theirs():
+                for n, N, K in LAYERS:
+                    torch.matmul(xs[K], self.W[n].t(), out=outs[n])
+            t_ours, t_cub = timeit(ours), timeit(theirs)
+            flops = sum(2.0 * M * N * K for _, N, K in LAYERS)
+            wbytes = sum(2.0 * (N * K + M * K + M * N) for _, N, K in LAYERS)
+            by_m[str(M)] = {"ms": round(t_ours, 4), "tflops": round(flops / t_ours / 1e9, 2),
+                            "gbs": round(wbytes / t_ours / 1e6, 1),
+                            "frac_of_measured_hbm": round(wbytes / t_ours / 1e6 / hbm, 4),
+                            "cublas_ms": round(t_cub, 4), "cost_vs_cublas": round(t_ours / t_cub, 4)}
+        res["gemm_by_m"] = by_m
         # fixed split COUNT attention (not batch-invariant), with the split
         # count a split-KV kernel would pick to fill 152 SMs at this batch
         ns = max(1, min(32, -(-2 * 152 // (ATT_B * HKV))))
@@ -394,6 +417,7 @@ def run_ours(args):
                         "flops_per_step": wl.gemm_flops,
                         "cublas_tflops_same_run": round(refs["cublas_tflops"], 2),
                         "cost_vs_cublas": round(refs["cublas_tflops"] / per_gpu_gemm, 4)},
+            "bi_gemm_by_m": refs["gemm_by_m"],
             "bi_decode_attention": {
                 "gbs": round(att_gbs / world, 1), "ms_per_step": round(att_ms / K, 4),
                 "frac_of_measured_hbm": round(att_gbs / world / hbm, 4),

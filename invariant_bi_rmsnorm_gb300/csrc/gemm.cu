@@ -22,6 +22,8 @@
 // are never stored; adding zero products leaves the other sums unchanged.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
 
@@ -58,10 +60,25 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            (uint64_t{1024 >> 4} << 32) | (uint64_t{1} << 46) | (uint64_t{2} << 61);
 }
 
+// Tile order (a schedule choice; every tile's arithmetic is the same in any
+// order): groups of `group_m` M-tiles, and within a group all N-tiles with the
+// M-tile fastest.  With group_m = all M-tiles this is plain m-fastest order;
+// a smaller group keeps a large activation operand's slice resident in L2
+// while the N-tiles sweep past it.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int& mb,
+                                            int& nb) {
+    const int per_group = group_m * num_n;
+    const int g = tile / per_group;
+    const int r = tile - g * per_group;
+    const int gm = min(group_m, num_m - g * group_m);
+    mb = g * group_m + r % gm;
+    nb = r / gm;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         const __grid_constant__ CUtensorMap tmap_w, __nv_bfloat16* __restrict__ y,
-                        int M, int N, int K, int64_t ld_y, uint32_t* err) {
+                        int M, int N, int K, int64_t ld_y, int group_m, uint32_t* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -105,7 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                const int mb = tile % num_m, nb = tile / num_m;
+                int mb, nb;
+                tile_coords(tile, num_m, num_n, group_m, mb, nb);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!bi::mbar_wait(&empty[stage], phase ^ 1)) {
                         bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmProducer);
@@ -171,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int mb = tile % num_m, nb = tile / num_m;
+            int mb, nb;
+            tile_coords(tile, num_m, num_n, group_m, mb, nb);
             if (!bi::mbar_wait(&tfull[acc], acc_phase)) {
                 if (lane == 0) bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmEpilogue);
                 break;
@@ -255,7 +274,13 @@ extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, i
     const int sms = bi::sm_count();
     if (sms <= 0) return BI_ERR_CUDA;
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    // keep at most ~64 MB of the activation operand resident per tile group
+    const int num_m = (M + BM - 1) / BM;
+    const int64_t slab = static_cast<int64_t>(BM) * K * 2;  // one M-tile's K extent
+    const int64_t budget = int64_t{64} << 20;
+    int group_m = num_m;
+    if (slab * num_m > budget) group_m = static_cast<int>(std::max<int64_t>(1, budget / slab));
     gemm_tcgen05_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-        tx, tw, static_cast<__nv_bfloat16*>(y), M, N, K, ld_y, bi::device_error_word());
+        tx, tw, static_cast<__nv_bfloat16*>(y), M, N, K, ld_y, group_m, bi::device_error_word());
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
