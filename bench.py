@@ -408,7 +408,7 @@ def run_ours(args):
             "traffic": gemm_traffic,
             "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                            else "fallback 1.9 PFLOP/s",
-            "kernel": "bi_gemm (gemm_tcgen05_kernel), 4 launches per step",
+            "kernel": "bi_gemm (gemm_tcgen05_pair_kernel), 4 launches per step",
         },
         "components": {
             "bi_gemm": {"tflops": round(per_gpu_gemm, 2), "ms_per_step": round(gemm_ms / K, 4),

@@ -115,14 +115,15 @@ bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y, 
  *
  * Operation: "2. Batch-Invariant Matrix Multiplication" of the same page: a
  * data-parallel tiled matmul with ONE kernel configuration for every shape --
- * a fixed 128x224 output tile, K walked in ascending 64-wide blocks, each
- * block as four ascending 16-deep tcgen05 MMAs accumulating in TMEM.  No
- * split-K or stream-K for any M, and the same MMA instruction shape always.
+ * a fixed 256x224 output tile computed by a pair of CTAs (tcgen05.mma
+ * cta_group::2, M=256, N=224, K=16), K walked in ascending 64-wide blocks,
+ * each block as four ascending 16-deep MMAs accumulating in TMEM.  No split-K
+ * or stream-K for any M, and the same MMA instruction shape always.
  *
  *   x  device, bf16 [M][ld_x] row-major (K contiguous).
  *   W  device, bf16 [N][ld_w] row-major: the nn.Linear weight layout.
  *   y  device, bf16 [M][ld_y] row-major; must not overlap x or W.
- *   M  0 .. 2^31-129;  N, K  >= 8 and multiples of 8.
+ *   M  0 .. 2^31-257;  N, K  >= 8 and multiples of 8.
  *   ld_x, ld_w, ld_y  in elements, multiples of 8, >= K, >= K, >= N.
  * Pointers must be 16-byte aligned.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
  * MISALIGNED, CUDA.

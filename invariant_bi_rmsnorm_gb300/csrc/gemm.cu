@@ -6,18 +6,22 @@
 // data-parallel matmul gives each output tile to one core and reduces its
 // whole K range there; splitting K when M*N is small, or switching tensor-core
 // instruction or tile shape with the batch size, changes the reduction order.
-// So this kernel has exactly one tile shape (128 x 224), one MMA instruction
-// shape (tcgen05.mma kind::f16, M=128, N=224, K=16) and one K order (64-wide
-// blocks ascending, each as 4 ascending 16-deep MMAs into one fp32 TMEM
-// accumulator), whatever M, N and K are.  No split-K, no stream-K.
+// So this kernel has exactly one tile shape (256 x 224, computed by a pair of
+// CTAs on two SMs), one MMA instruction shape (tcgen05.mma.cta_group::2
+// kind::f16, M=256, N=224, K=16) and one K order (64-wide blocks ascending,
+// each as 4 ascending 16-deep MMAs into one fp32 TMEM accumulator), whatever
+// M, N and K are.  No split-K, no stream-K.
 //
-// Structure (persistent, one CTA per SM, warp-specialised):
-//   warp 0      TMA producer: x and W tiles (128x64 and 224x64 bf16, 128-byte
-//               swizzle) into a 5-stage shared-memory ring;
-//   warp 1      allocates 512 TMEM columns (two 128x224 fp32 accumulators) and
-//               issues the MMAs from one thread;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32*(w%4) ..), fp32 -> bf16 round-to-nearest-even, store.
+// Structure (persistent, one CTA pair per two SMs, warp-specialised):
+//   warp 0      TMA producer in each CTA: its 128 rows of x and its 112 rows
+//               of W (64-wide K slabs, 128-byte swizzle) into a 7-stage ring;
+//               both CTAs' copies complete on the leader CTA's barrier;
+//   warp 1      allocates 512 TMEM columns in both CTAs (two accumulators);
+//               in the leader CTA one thread issues the pair MMAs, which read
+//               both CTAs' shared memory, so each SM streams half of the W tile;
+//   warps 2..5  epilogue in each CTA: tcgen05.ld of its own 128 rows of the
+//               accumulator (warp w reads TMEM lanes 32*(w%4) ..), fp32 -> bf16
+//               round-to-nearest-even, store.
 // Rows past M and columns past N read as zeros (TMA out-of-bounds fill) and
 // are never stored; adding zero products leaves the other sums unchanged.
 #include <cuda_bf16.h>
@@ -28,27 +32,6 @@
 #include "bi_ptx.cuh"
 
 namespace {
-
-constexpr int BM = 128;
-constexpr int BN = 224;  // N = 224 keeps whole waves on 152 SMs for the usual layer widths
-constexpr int BK = 64;
-constexpr int kStages = 5;
-constexpr int kABytes = BM * BK * 2;  // 16 KiB
-constexpr int kBBytes = BN * BK * 2;  // 28 KiB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;  // two accumulators, at columns 0 and 256
-constexpr uint32_t kAccStride = 256;
-static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
-static_assert(BN % 16 == 0 && BN <= 256 && BN <= static_cast<int>(kAccStride), "tcgen05 M=128 shape");
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9
-// = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
-// bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
 
 // Shared-memory matrix descriptor for a K-major tile stored as 128-byte rows
 // with the 128-byte swizzle: start address >> 4 (bits 0-13), leading byte
@@ -75,10 +58,39 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     nb = r / gm;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                        const __grid_constant__ CUtensorMap tmap_w, __nv_bfloat16* __restrict__ y,
-                        int M, int N, int K, int64_t ld_y, int group_m, uint32_t* err) {
+namespace pair {
+constexpr int BMP = 256;  // pair tile rows
+constexpr int BMC = 128;  // rows per CTA
+constexpr int BN = 224;
+constexpr int BNC = BN / 2;  // W rows per CTA
+constexpr int BK = 64;
+constexpr int kStages = 7;
+constexpr int kABytes = BMC * BK * 2;  // 16 KiB
+constexpr int kBBytes = BNC * BK * 2;  // 14 KiB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle alignment");
+static_assert(BN % 16 == 0 && BN <= 256 && BN <= static_cast<int>(kAccStride), "tcgen05 shape");
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9
+// = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
+// bits 17-22, M >> 4 at bits 24-28 (M = 256: the pair's rows).
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BMP >> 4) << 24);
+}  // namespace pair
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
+    gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                             const __grid_constant__ CUtensorMap tmap_w,
+                             __nv_bfloat16* __restrict__ y, int M, int N, int K, int64_t ld_y,
+                             int group_m, uint32_t* err) {
+    constexpr int BMP = pair::BMP, BMC = pair::BMC, BN = pair::BN, BNC = pair::BNC, BK = pair::BK;
+    constexpr int kStages = pair::kStages, kABytes = pair::kABytes, kStageBytes = pair::kStageBytes;
+    constexpr uint32_t kTmemCols = pair::kTmemCols, kAccStride = pair::kAccStride;
+    constexpr uint32_t kIdesc = pair::kIdesc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -88,32 +100,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
+    const uint32_t rank = bi::cluster_ctarank();
+    const bool leader = rank == 0;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_m = (M + BM - 1) / BM;
+    const int num_m = (M + BMP - 1) / BMP;
     const int num_n = (N + BN - 1) / BN;
     const int num_tiles = num_m * num_n;
     const int num_kb = (K + BK - 1) / BK;
+    const int pair_id = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            bi::mbar_init(&full[i], 1);
-            bi::mbar_init(&empty[i], 1);
+            bi::mbar_init(&full[i], 1);   // the leader's arrive (+ both CTAs' bytes)
+            bi::mbar_init(&empty[i], 1);  // one pair-MMA commit
         }
         for (int i = 0; i < 2; ++i) {
             bi::mbar_init(&tfull[i], 1);
-            bi::mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
+            bi::mbar_init(&tempty[i], 8);  // 4 epilogue warps in each CTA (leader's copy used)
         }
         bi::fence_mbar_init();
         bi::tma_prefetch_desc(&tmap_x);
         bi::tma_prefetch_desc(&tmap_w);
     }
     if (warp == 1) {
-        bi::tmem_alloc(tmem_slot, kTmemCols);
-        bi::tmem_relinquish();
+        bi::tmem_alloc_pair(tmem_slot, kTmemCols);
+        bi::tmem_relinquish_pair();
     }
     bi::tc_fence_before();
-    __syncthreads();
+    bi::cluster_sync();  // both CTAs' barriers exist before either signals the other
     bi::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -121,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int tile = pair_id; tile < num_tiles; tile += npairs) {
                 int mb, nb;
                 tile_coords(tile, num_m, num_n, group_m, mb, nb);
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -130,9 +146,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         goto producer_done;
                     }
                     uint8_t* sa = smem + stage * kStageBytes;
-                    bi::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-                    bi::tma_load_2d(sa, &tmap_x, &full[stage], kb * BK, mb * BM);
-                    bi::tma_load_2d(sa + kABytes, &tmap_w, &full[stage], kb * BK, nb * BN);
+                    const uint32_t full_leader = bi::mapa_shared(bi::smem_u32(&full[stage]), 0);
+                    if (leader) bi::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                    bi::tma_load_2d_pair(sa, &tmap_x, full_leader, kb * BK,
+                                         mb * BMP + static_cast<int>(rank) * BMC);
+                    bi::tma_load_2d_pair(sa + kABytes, &tmap_w, full_leader, kb * BK,
+                                         nb * BN + static_cast<int>(rank) * BNC);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -142,12 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         producer_done:;
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int tile = pair_id; tile < num_tiles; tile += npairs) {
                 if (!bi::mbar_wait(&tempty[acc], acc_phase ^ 1)) {
                     bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmMma);
                     break;
@@ -166,17 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sb = sa + kABytes;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        bi::tc_mma_f16(d_tmem, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k),
-                                       kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        bi::tc_mma_f16_pair(d_tmem, sw128_desc(sa + 32 * k),
+                                            sw128_desc(sb + 32 * k), kIdesc,
+                                            (kb | k) != 0 ? 1u : 0u);
                     }
-                    bi::tc_commit(&empty[stage]);  // stage free once these MMAs finish
+                    bi::tc_commit_pair_multicast(&empty[stage], 0x3);  // stage free in both CTAs
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                bi::tc_commit(&tfull[acc]);  // accumulator ready for the epilogue
+                bi::tc_commit_pair_multicast(&tfull[acc], 0x3);  // both halves of D ready
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1;
@@ -184,11 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // epilogue warps 2..5 -> TMEM lane quarter warp % 4
+        // epilogue warps 2..5 -> TMEM lane quarter warp % 4 of this CTA's 128 rows
         const int quarter = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int tile = pair_id; tile < num_tiles; tile += npairs) {
             int mb, nb;
             tile_coords(tile, num_m, num_n, group_m, mb, nb);
             if (!bi::mbar_wait(&tfull[acc], acc_phase)) {
@@ -196,10 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             bi::tc_fence_after();
-            const int row = mb * BM + quarter * 32 + lane;
+            const int row = mb * BMP + static_cast<int>(rank) * BMC + quarter * 32 + lane;
             __nv_bfloat16* yrow = y + static_cast<int64_t>(row) * ld_y;
-            const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc) * kAccStride;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc) * kAccStride;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 const int col0 = nb * BN + ch * 32;
@@ -222,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bi::tc_fence_before();
             __syncwarp();
-            if (lane == 0) bi::mbar_arrive(&tempty[acc]);
+            if (lane == 0) bi::mbar_arrive_cluster(bi::mapa_shared(bi::smem_u32(&tempty[acc]), 0));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1;
@@ -231,10 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     bi::tc_fence_before();
-    __syncthreads();
+    bi::cluster_sync();  // both CTAs past their last TMEM access and remote arrive
     if (warp == 1) {
         bi::tc_fence_after();
-        bi::tmem_dealloc(tmem_base, kTmemCols);
+        bi::tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -246,7 +266,7 @@ extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, i
                              int32_t K, int64_t ld_x, int64_t ld_w, int64_t ld_y,
                              cudaStream_t stream) {
     if (M < 0 || N < 8 || K < 8) return M < 0 ? BI_ERR_INVALID_ARG : BI_ERR_UNSUPPORTED_SHAPE;
-    if (M > 0x7fffffff - BM) return BI_ERR_UNSUPPORTED_SHAPE;  // row indices stay in int
+    if (M > 0x7fffffff - pair::BMP) return BI_ERR_UNSUPPORTED_SHAPE;  // row indices stay in int
     if ((N & 7) || (K & 7)) return BI_ERR_UNSUPPORTED_SHAPE;
     if (ld_x < K || ld_w < K || ld_y < N) return BI_ERR_INVALID_ARG;
     if ((ld_x & 7) || (ld_w & 7) || (ld_y & 7)) return BI_ERR_MISALIGNED;
@@ -254,33 +274,36 @@ extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, i
     if (!x || !W || !y) return BI_ERR_INVALID_ARG;
     if (!bi::aligned16(x) || !bi::aligned16(W) || !bi::aligned16(y)) return BI_ERR_MISALIGNED;
 
+    // TMA boxes: each CTA loads 128 rows of x and 112 rows of W per 64-wide K slab
     CUtensorMap tx, tw;
     if (bi::encode_tensor_map_2d(&tx, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                                 static_cast<uint64_t>(ld_x) * 2, BK, BM) != CUDA_SUCCESS ||
+                                 static_cast<uint64_t>(ld_x) * 2, pair::BK, pair::BMC) != CUDA_SUCCESS ||
         bi::encode_tensor_map_2d(&tw, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                                 static_cast<uint64_t>(ld_w) * 2, BK, BN) != CUDA_SUCCESS)
+                                 static_cast<uint64_t>(ld_w) * 2, pair::BK, pair::BNC) != CUDA_SUCCESS)
         return BI_ERR_CUDA;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BI_ERR_CUDA;
     if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_tcgen05_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 pair::kSmemBytes) != cudaSuccess)
             return BI_ERR_CUDA;
         g_attr_set[dev] = true;
     }
-    const int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    if (tiles > 0x7fffffffLL) return BI_ERR_UNSUPPORTED_SHAPE;
     const int sms = bi::sm_count();
-    if (sms <= 0) return BI_ERR_CUDA;
-    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-    // keep at most ~64 MB of the activation operand resident per tile group
-    const int num_m = (M + BM - 1) / BM;
-    const int64_t slab = static_cast<int64_t>(BM) * K * 2;  // one M-tile's K extent
+    if (sms < 2) return BI_ERR_CUDA;
+    const int num_m = (M + pair::BMP - 1) / pair::BMP;
+    const int64_t tiles = static_cast<int64_t>(num_m) * ((N + pair::BN - 1) / pair::BN);
+    if (tiles > 0x7fffffffLL) return BI_ERR_UNSUPPORTED_SHAPE;
+    const int pairs = static_cast<int>(tiles < sms / 2 ? tiles : sms / 2);
+    // Tile order: keep at most ~64 MB of the activation operand per group of
+    // M-tiles, so a large x stays L2-resident while the N-tiles sweep past it.
+    const int64_t slab = static_cast<int64_t>(pair::BMP) * K * 2;
     const int64_t budget = int64_t{64} << 20;
     int group_m = num_m;
     if (slab * num_m > budget) group_m = static_cast<int>(std::max<int64_t>(1, budget / slab));
-    gemm_tcgen05_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
+    gemm_tcgen05_pair_kernel<<<2 * pairs, pair::kThreads, pair::kSmemBytes, stream>>>(
         tx, tw, static_cast<__nv_bfloat16*>(y), M, N, K, ld_y, group_m, bi::device_error_word());
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
