@@ -65,8 +65,11 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the cold-L2 timings of the kernels beyond the bench step")
     ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "gemm_layers", "attention",
-                                       "rmsnorm", "decoder"],
+                                       "rmsnorm", "decoder", "prefill", "add_rmsnorm",
+                                       "logprobs", "qk_norm_rope_append", "silu_mul"],
                     help="time one kernel of the path alone (for profiling); prints its own line")
     ap.add_argument("--requests", type=int, default=1000, help="--case decoder: requests")
     ap.add_argument("--layers", type=int, default=36, help="--case decoder: decoder layers")
@@ -87,14 +90,41 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+KERNEL_SOURCES = {"bi_gemm": "gemm.cu", "bi_decode_attention": "decode_attention.cu",
+                  "bi_rmsnorm": "rmsnorm.cu", "bi_add_rmsnorm": "rmsnorm.cu",
+                  "bi_prefill_attention": "prefill_attention.cu", "bi_logprobs": "logprobs.cu",
+                  "bi_qk_norm_rope_append": "decoder_ops.cu", "bi_silu_mul": "decoder_ops.cu"}
+
+
+def kernel_source_sha(src: str) -> str:
+    """sha256[:16] of a kernel's .cu file followed by every header of the
+    package it includes (transitively, each once, in first-include order)."""
+    import re
+    csrc = os.path.join(ROOT, "invariant_bi_rmsnorm_gb300", "csrc")
+    inc = os.path.join(ROOT, "include")
+    h = hashlib.sha256()
+    seen, todo = set(), [os.path.join(csrc, src)]
+    while todo:
+        path = todo.pop(0)
+        if path in seen:
+            continue
+        seen.add(path)
+        text = open(path, "rb").read()
+        h.update(text)
+        for name in re.findall(rb'#include "([^"]+)"', text):
+            for d in (os.path.dirname(path), csrc, inc):
+                cand = os.path.join(d, name.decode())
+                if os.path.exists(cand):
+                    todo.append(os.path.normpath(cand))
+                    break
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel: str):
     """dram bytes per launch from the committed ncu summary, if it was taken
     on the current source of that kernel (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
-    src = {"bi_gemm": "gemm.cu", "bi_decode_attention": "decode_attention.cu",
-           "bi_rmsnorm": "rmsnorm.cu"}[kernel]
-    sha = hashlib.sha256(open(os.path.join(ROOT, "invariant_bi_rmsnorm_gb300", "csrc", src),
-                              "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha(KERNEL_SOURCES[kernel])
     if not os.path.exists(p):
         return None
     for line in open(p):
@@ -281,6 +311,60 @@ class Workload:
                 "bi_gemm_rows_differing_M64_vs_M4096_of_64": rows(ours_small, ours_big[:64]),
                 "torch_rms_norm_row0_differs_B1_vs_B4096": bool(rows(r_small, r_big[:1]))}
 
+    def next_rows(self, reps: int = 10):
+        """Cold-L2 timings (outside the timed steps) of the decode-attention
+        batch sweep and of the kernels beyond the step: prefill attention, the
+        fused residual add + RMSNorm, log-probabilities, and the decoder's
+        per-token ops.  Each with its roofline fraction and, for attention, the
+        same-batch fixed-split-count reference."""
+        from invariant_bi_rmsnorm_gb300 import inputs
+        hbm, bf16 = load_peaks()[:2]
+        flush = torch.ones(64 << 20, dtype=torch.int32, device=self.dev)
+        res = {"l2": "a 256 MB buffer is read before every launch (L2 left clean and cold); "
+                     f"mean of {reps} launches"}
+        a = self.att
+        by_b = {}
+        for B in (1, 16, 128):
+            lens = self.att_lens[:B]
+            nbytes = float((lens * HKV * HD * 4).sum() + B * HQ * HD * 4 + 4 * ((lens + 15) // 16).sum() + 4 * B)
+            q, bt, sl = a["q"][:B], a["block_table"][:B], a["seq_lens"][:B]
+            out = torch.empty(B, HQ, HD, dtype=torch.bfloat16, device=self.dev)
+            t = time_cold(lambda: self.bi.decode_attention(
+                q, a["k_cache"], a["v_cache"], bt, sl, max_seq_len=MAX_LEN, out=out,
+                workspace=self.ws), reps, flush)
+            ns = max(1, min(32, -(-2 * 152 // (B * HKV))))
+            ws = torch.empty(self.bi.decode_attention_workspace_size(B, HQ, HD, ns * 256),
+                             dtype=torch.uint8, device=self.dev)
+            t_fc = time_cold(lambda: self.bi.decode_attention_fixed_splits(
+                q, a["k_cache"], a["v_cache"], bt, sl, MAX_LEN, ns, out=out, workspace=ws),
+                reps, flush)
+            by_b[str(B)] = {"ms": round(t, 4), "gbs": round(nbytes / t / 1e6, 1),
+                            "frac_of_measured_hbm": round(nbytes / t / 1e6 / hbm, 4),
+                            "kv_tokens": int(lens.sum()),
+                            "fixed_split_count": ns, "fixed_split_count_ms": round(t_fc, 4),
+                            "cost_vs_fixed_split_count": round(t / t_fc, 4)}
+        res["bi_decode_attention_by_batch"] = by_b
+        for name in NEXT_CASES:
+            fn, work, unit, info = build_next_case(name, self.dev, self.bi, inputs)
+            t = time_cold(fn, reps, flush)
+            rate = work / (t * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+            entry = {"ms": round(t, 4), ("tflops" if unit == "TFLOP/s" else "gbs"): round(rate, 2)}
+            if unit == "TFLOP/s":
+                entry["frac_of_measured_bf16_burst"] = round(rate / bf16, 4)
+                entry["gbs"] = round(info.pop("bytes") / t / 1e6, 1)
+                entry["bound"] = "tensor (mma.sync m16n8k16, not tcgen05)"
+            else:
+                entry["frac_of_measured_hbm"] = round(rate / hbm, 4)
+                entry["bound"] = "hbm"
+            entry["traffic"] = traffic_record("bi_" + name if name != "prefill"
+                                              else "bi_prefill_attention")
+            entry.update(info)
+            res["bi_" + name if name != "prefill" else "bi_prefill_attention"] = entry
+            del fn
+        torch.cuda.synchronize()
+        self.bi.get_device_error()
+        return res
+
     def references(self, reps: int = 5):
         """Same-run timings of the non-invariant library references."""
         import torch.nn.functional as F
@@ -362,6 +446,7 @@ def run_ours(args):
     invariant = wl.invariance()
     controls = wl.negative_controls()
     refs = wl.references()
+    extra = wl.next_rows() if not args.no_next_rows else None
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -453,6 +538,7 @@ def run_ours(args):
                 "traffic": traffic_record("bi_rmsnorm")},
         },
         "bitwise_invariant": all(invariant.values()),
+        **({"next_rows": extra} if extra is not None else {}),
         "invariance_checks": invariant,
         "negative_controls": controls,
         "clocks": clk,
@@ -661,6 +747,103 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PREFILL_BUDGET = 8192  # tokens of one prefill step
+LOGPROB_ROWS, VOCAB = 1024, 151936
+OPS_TOKENS = 8192
+
+
+def build_next_case(name: str, dev, bi, inputs):
+    """Full-size input of one kernel beyond the bench step, as (fn, work, unit,
+    info).  `work` is the algorithmic bytes (GB/s cases) or FLOPs (TFLOP/s)
+    of one launch.  Shared by the default line's cold-L2 measurements and by
+    `--case` (the command the ncu captures use)."""
+    if name == "prefill":
+        # one step of whole-prompt prefill: prompts of U[32, 512] tokens until
+        # the 8192-token budget is full, causal attention over each prompt
+        lens_all = inputs.seq_lens_uniform(64, 512, seed=610, min_len=32).tolist()
+        lens, tot = [], 0
+        for L in lens_all:
+            if tot + L > PREFILL_BUDGET:
+                break
+            lens.append(L)
+            tot += L
+        p = inputs.decode_problem(len(lens), Hq=HQ, Hkv=HKV, D=HD, seq_lens=lens, seed=611,
+                                  device=dev)
+        q = inputs.normal_bf16((tot, HQ, HD), 612, device=dev)
+        a = {k: v.to(dev) for k, v in p.items() if k != "q"}
+        indptr = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+        out = torch.empty(tot, HQ, HD, dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.prefill_attention(q, a["k_cache"], a["v_cache"], a["block_table"],  # noqa: E731
+                                          a["seq_lens"], indptr, max_q_len=max(lens),
+                                          max_seq_len=max(lens), out=out)
+        flops = float(sum(4.0 * HD * HQ * L * (L + 1) / 2 for L in lens))
+        nbytes = float(2 * tot * HQ * HD * 2 + sum(L * HKV * HD * 4 for L in lens))
+        return fn, flops, "TFLOP/s", {"sequences": len(lens), "tokens": tot,
+                                      "prompt_len": "U[32,512]", "bytes": nbytes}
+    if name == "add_rmsnorm":
+        x = inputs.rmsnorm_rows(RMS_ROWS, HIDDEN, seed=3, device=dev)
+        res = inputs.rmsnorm_rows(RMS_ROWS, HIDDEN, seed=13, device=dev)
+        w = inputs.rmsnorm_weight(HIDDEN, seed=4, device=dev)
+        y = torch.empty_like(x)
+        fn = lambda: bi.add_rmsnorm(x, res, w, EPS, out=y)  # noqa: E731
+        return fn, 4.0 * 2 * RMS_ROWS * HIDDEN + 2 * HIDDEN, "GB/s", {
+            "rows": RMS_ROWS, "hidden": HIDDEN,
+            "bytes_per_row": "x read, residual read + write, y write"}
+    if name == "logprobs":
+        logits = inputs.normal_bf16((LOGPROB_ROWS, VOCAB), 620, device=dev)
+        tgt = torch.randint(0, VOCAB, (LOGPROB_ROWS,), generator=torch.Generator().manual_seed(621),
+                            dtype=torch.int64).to(torch.int32).to(dev)
+        fn = lambda: bi.logprobs(logits, tgt)  # noqa: E731
+        return fn, float(LOGPROB_ROWS * VOCAB * 2 + LOGPROB_ROWS * 12), "GB/s", {
+            "rows": LOGPROB_ROWS, "vocab": VOCAB}
+    if name == "qk_norm_rope_append":
+        T = OPS_TOKENS
+        qkv = inputs.normal_bf16((T, (HQ + 2 * HKV) * HD), 630, device=dev)
+        npages = T // 16
+        kc = torch.empty(npages, HKV, 16, HD, dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        g = torch.Generator().manual_seed(631)
+        pos = torch.randint(0, 8192, (T,), generator=g, dtype=torch.int64).to(torch.int32).to(dev)
+        slots = torch.randperm(npages * 16, generator=g).to(torch.int32).to(dev)
+        rope = bi.rope_table(8192, 1e6, HD, device=dev)
+        ones = torch.ones(HD, dtype=torch.bfloat16, device=dev)
+        qo = torch.empty(T, HQ, HD, dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.qk_norm_rope_append(qkv, HQ, HKV, pos, slots, rope, ones, ones,  # noqa: E731
+                                            kc, vc, EPS, q_out=qo)
+        per_tok = (HQ + 2 * HKV) * HD * 2 + HQ * HD * 2 + 2 * HKV * HD * 2 + HD * 4 + 8
+        return fn, float(T * per_tok), "GB/s", {
+            "tokens": T, "bytes_per_token": "qkv read, q write, k/v cache write, rope row, "
+                                           "position and slot"}
+    if name == "silu_mul":
+        T, F = OPS_TOKENS, 12288
+        gu = inputs.normal_bf16((T, 2 * F), 640, device=dev)
+        h = torch.empty(T, F, dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.silu_mul(gu, out=h)  # noqa: E731
+        return fn, float(T * 3 * F * 2), "GB/s", {"tokens": T, "ffn": F}
+    raise ValueError(name)
+
+
+NEXT_CASES = ("prefill", "add_rmsnorm", "logprobs", "qk_norm_rope_append", "silu_mul")
+
+
+def time_cold(fn, reps: int, flush: torch.Tensor) -> float:
+    """Mean device time (ms) of fn over reps launches, L2 flushed before each
+    by reading a buffer twice the size of L2 (outside the timed events).  A
+    read leaves clean lines behind; overwriting the buffer instead would leave
+    L2 full of dirty lines whose write-back the timed kernel would pay for."""
+    fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for e0, e1 in evs:
+        torch.sum(flush)
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / reps
+
+
 def run_case(args):
     """One kernel of the path, launched steps + warmup times on its full-size
     input: the small, self-contained command the ncu captures use."""
@@ -686,6 +869,8 @@ def run_case(args):
         W = inputs.gemm_weight(N, K, seed=42, device=dev)
         y = torch.empty(GEMM_M, N, dtype=torch.bfloat16, device=dev)
         fn, work, unit = (lambda: bi.gemm(x, W, out=y)), 2.0 * GEMM_M * N * K, "TFLOP/s"
+    elif args.case in NEXT_CASES:
+        fn, work, unit, _ = build_next_case(args.case, dev, bi, inputs)
     elif args.case == "attention":
         B = args.batch
         p = inputs.decode_problem(B, max_len=MAX_LEN, seed=270, device=dev)

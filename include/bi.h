@@ -286,9 +286,10 @@ bi_status bi_silu_mul(const void* gate_up, int64_t ld_gate_up, int32_t T, int32_
  * LLM Inference: The Core Role of Batch Invariance" ("Experimental Validation
  * and Future Prospects", true on-policy RL) needs: the softmax denominator is
  * a reduction over the vocabulary, computed one row per CTA in an order that
- * depends only on `vocab` (max, then sum of exp(x - max) over fixed per-thread
- * strides, a warp butterfly and a warp-ordered fold), so a row's results are
- * bit-identical in any batch.
+ * depends only on `vocab` (one pass: each thread folds its fixed stride of
+ * 8-value vectors into a running max and sum of exp(x - max); then a warp
+ * butterfly and a warp-ordered fold of those pairs), so a row's results are
+ * bit-identical in any batch.  -inf logits (a masked vocabulary) add nothing.
  *   logits   device, bf16 [rows][ld], ld >= vocab, both multiples of 8.
  *   targets  device, int32 [rows] or null;  logprob_out  device, fp32 [rows]
  *            (needed with targets);  lse_out  device, fp32 [rows] or null.

@@ -51,13 +51,17 @@ using bi_attn::kPagesPerChunk;
 using bi_attn::kStageBytes;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStagesPerWarp = 2;
-constexpr int kStages = kWarps * kStagesPerWarp;
 constexpr int kMaxPagesPerCta = 512;                                // pages one CTA walks
 constexpr int kMaxChunksPerCta = kMaxPagesPerCta / kPagesPerChunk;  // 32
 constexpr int kFoldFloats = kMaxGroup * kD + 2 * kMaxGroup;          // running fold (O, M, L)
+// Pages in flight per warp (its private TMA ring): 72.8 KB per CTA, 3 CTAs
+// per SM.  A six-deep ring (one CTA per SM) was measured as no faster at one
+// sequence and slower from eight sequences up: a warp's chunk is paced by its
+// per-page arithmetic, not by HBM latency.
+constexpr int kSPW = 2;
+constexpr int kStages = kWarps * kSPW;
 constexpr int kSmemBytes = kStages * kStageBytes + kFoldFloats * 4 + 4 * kMaxPagesPerCta +
-                           8 * kStages + 1024 /*align*/;  // 71.2 KB: 3 CTAs per SM
+                           8 * kStages + 1024 /*align*/;
 
 struct SplitArgs {
     const __nv_bfloat16* q;
@@ -150,14 +154,14 @@ __global__ void __launch_bounds__(kThreads)
     auto stage_ptr = [&](int st) { return smem + st * kStageBytes; };
 
     // This warp's pages, in order: chunk c0 + warp, its pages 0, 1, ...; then
-    // chunk c0 + warp + 4, ...  The loader runs two pages ahead of the compute
-    // loop through this warp's 2-stage ring; every lane tracks the loader
-    // position, lane 0 issues the copies.
+    // chunk c0 + warp + 4, ...  The loader runs kSPW pages ahead of the
+    // compute loop through this warp's kSPW-stage ring; every lane tracks the
+    // loader position, lane 0 issues the copies.
     int lc = c0 + warp, lp = 0, lj = 0;
     auto issue_next = [&]() {
         if (lc >= c1) return;
         if (lane == 0) {
-            const int st = warp * kStagesPerWarp + (lj & 1);
+            const int st = warp * kSPW + lj % kSPW;
             uint8_t* kd = stage_ptr(st);
             uint8_t* vd = kd + kMatBytes;
             const int row = rows_s[(lc - c0) * ppc + lp];
@@ -173,8 +177,8 @@ __global__ void __launch_bounds__(kThreads)
             lp = 0;
         }
     };
-    issue_next();
-    issue_next();
+#pragma unroll
+    for (int i = 0; i < kSPW; ++i) issue_next();
 
     // column n of the mma tile = query head g*group + n (n < group)
     uint32_t qb0[8], qb1[8];
@@ -196,9 +200,9 @@ __global__ void __launch_bounds__(kThreads)
         if (c < c1) {
             const int np = pages_in(c);
             for (int p = 0; p < np; ++p, ++j) {
-                const int stg = warp * kStagesPerWarp + (j & 1);
+                const int stg = warp * kSPW + j % kSPW;
                 if (timed_out) continue;
-                if (!bi::mbar_wait(&bars[stg], (j >> 1) & 1)) {
+                if (!bi::mbar_wait(&bars[stg], (j / kSPW) & 1)) {
                     timed_out = true;
                     continue;
                 }
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(kThreads)
                 const uint32_t kb = bi::smem_u32(stage_ptr(stg));
                 bi_attn::attend_page(st, kb, kb + kMatBytes, qb0, qb1, valid, valid, a.scale_log2,
                                      lane);
-                // hand the stage back to TMA for this warp's page two ahead
+                // hand the stage back to TMA for this warp's page kSPW ahead
                 bi::fence_proxy_async_smem();
                 __syncwarp();
                 issue_next();
@@ -313,15 +317,29 @@ __global__ void __launch_bounds__(kD)
     float M = ws_ml[base * 2];
     float Ls = ws_ml[base * 2 + 1];
     float A = ws_acc[base * kD + d];
-    for (int c = 1; c < nch; ++c) {
-        const float mc = ws_ml[(base + c) * 2];
-        const float lc = ws_ml[(base + c) * 2 + 1];
-        const float ac = ws_acc[(base + c) * kD + d];
-        float Mn, fo, fc;
-        bi_attn::fold_scalars(M, mc, Mn, fo, fc);
-        Ls = bi_attn::fold_value(Ls, fo, lc, fc);
-        A = bi_attn::fold_value(A, fo, ac, fc);
-        M = Mn;
+    // the loads of up to kBatch chunks are issued before any of them is
+    // folded (the fold itself stays strictly sequential in c)
+    constexpr int kBatch = 8;
+    for (int cb = 1; cb < nch; cb += kBatch) {
+        float mc[kBatch], lc[kBatch], ac[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (cb + i < nch) {
+                const int64_t pc = base + cb + i;
+                mc[i] = ws_ml[pc * 2];
+                lc[i] = ws_ml[pc * 2 + 1];
+                ac[i] = ws_acc[pc * kD + d];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (cb + i >= nch) break;
+            float Mn, fo, fc;
+            bi_attn::fold_scalars(M, mc[i], Mn, fo, fc);
+            Ls = bi_attn::fold_value(Ls, fo, lc[i], fc);
+            A = bi_attn::fold_value(A, fo, ac[i], fc);
+            M = Mn;
+        }
     }
     out[(static_cast<int64_t>(s) * Hq + hq) * kD + d] = __float2bfloat16_rn(__fdiv_rn(A, Ls));
 }
@@ -406,8 +424,8 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
         return BI_ERR_CUDA;
 
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BI_ERR_CUDA;
-    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
+    if (!g_attr_set[dev]) {
         if (cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
             return BI_ERR_CUDA;
@@ -446,7 +464,6 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     }
     args.chunks_per_cta = cpc;
     const int groups = ceil_div(max_chunks, cpc);
-
     attn_split_kernel<<<dim3(groups, Hkv, B), kThreads, kSmemBytes, stream>>>(tk, tv, args);
     if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
     if (max_chunks > cpc) {

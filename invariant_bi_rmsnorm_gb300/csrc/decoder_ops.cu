@@ -20,7 +20,6 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kHalf = kD / 2;
-constexpr int kWarpsPerBlock = 4;
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
 
@@ -43,73 +42,103 @@ struct RopeArgs {
     uint32_t* err;
 };
 
-// One warp per (token, head).  Lane l holds dims 2l, 2l+1 (first half) and
-// 64+2l, 64+2l+1 (their rotation partners).
+// One CTA of 8 warps per token; warp w takes heads w, w+8, w+16, ... and
+// issues the loads of up to kHeadsPerPass of them before computing any, so
+// enough bytes are in flight to cover HBM latency.  Per head, lane l holds
+// dims 2l, 2l+1 (first half) and 64+2l, 64+2l+1 (their rotation partners):
 //   q, k heads:  x -> bf16(x * rsqrt(mean(x^2) + eps) * w)   (if a norm weight is given;
 //                    sum of squares: per lane in the order 2l, 2l+1, 64+2l, 64+2l+1, then
 //                    an xor butterfly over lanes)
 //                -> rotate-half RoPE in fp32: y_i = x_i c_i - x_{64+i} s_i,
 //                   y_{64+i} = x_{64+i} c_i + x_i s_i, rounded once to bf16
 //   v heads:     copied.
-// q goes to q_out; k and v to their token's cache slot.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) qk_norm_rope_append_kernel(const RopeArgs a) {
-    const int warp_global = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+// q goes to q_out; k and v to their token's cache slot.  Each head's
+// arithmetic depends only on its own 128 values, the position and the weights.
+constexpr int kRopeWarps = 8;
+constexpr int kHeadsPerPass = 6;
+
+__device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
+__global__ void __launch_bounds__(kRopeWarps * 32) qk_norm_rope_append_kernel(const RopeArgs a) {
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int heads = a.Hq + 2 * a.Hkv;
-    if (warp_global >= a.T * heads) return;
-    const int t = warp_global / heads;
-    const int h = warp_global % heads;
     const int pos = a.positions[t];
     const int64_t slot = a.slots[t];
     if (pos < 0 || pos >= a.max_pos || slot < 0 || slot >= a.num_slots) {
-        if (lane == 0 && h == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereDecoderOps);
+        if (threadIdx.x == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereDecoderOps);
         return;
     }
-    const __nv_bfloat16* src = a.qkv + static_cast<int64_t>(t) * a.ld_qkv + static_cast<int64_t>(h) * kD;
     const int i0 = 2 * lane;
-    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(src + i0);
-    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(src + kHalf + i0);
-    float x[4] = {__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi)};
-
-    const int64_t page = slot / a.page_size, off = slot % a.page_size;
-    if (h >= a.Hq + a.Hkv) {  // v: copy into the cache
-        const int hv = h - a.Hq - a.Hkv;
-        __nv_bfloat16* dst = a.v_cache + ((page * a.Hkv + hv) * a.page_size + off) * kD;
-        *reinterpret_cast<__nv_bfloat162*>(dst + i0) = lo;
-        *reinterpret_cast<__nv_bfloat162*>(dst + kHalf + i0) = hi;
-        return;
-    }
-    const bool is_q = h < a.Hq;
-    const __nv_bfloat16* nw = is_q ? a.q_norm_w : a.k_norm_w;
-    if (nw) {
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) ss = __fmaf_rn(x[e], x[e], ss);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float r = rsqrtf(__fdiv_rn(ss, static_cast<float>(kD)) + a.eps);
-        const int idx[4] = {i0, i0 + 1, kHalf + i0, kHalf + i0 + 1};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            x[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(x[e], r), bf(nw[idx[e]]))));
-    }
     const float* cs = a.rope + static_cast<int64_t>(pos) * kD;
-    float y[4];
+    const float2 cosv = *reinterpret_cast<const float2*>(cs + i0);
+    const float2 sinv = *reinterpret_cast<const float2*>(cs + kHalf + i0);
+    const float c[2] = {cosv.x, cosv.y}, sn[2] = {sinv.x, sinv.y};
+    const int idx[4] = {i0, i0 + 1, kHalf + i0, kHalf + i0 + 1};
+    float qw[4], kw[4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const float c = cs[i0 + e], sn = cs[kHalf + i0 + e];
-        y[e] = __fsub_rn(__fmul_rn(x[e], c), __fmul_rn(x[2 + e], sn));
-        y[2 + e] = __fadd_rn(__fmul_rn(x[2 + e], c), __fmul_rn(x[e], sn));
+    for (int e = 0; e < 4; ++e) {
+        qw[e] = a.q_norm_w ? bf(a.q_norm_w[idx[e]]) : 0.f;
+        kw[e] = a.k_norm_w ? bf(a.k_norm_w[idx[e]]) : 0.f;
     }
-    __nv_bfloat16* dst;
-    if (is_q) {
-        dst = a.q_out + (static_cast<int64_t>(t) * a.Hq + h) * kD;
-    } else {
-        const int hk = h - a.Hq;
-        dst = a.k_cache + ((page * a.Hkv + hk) * a.page_size + off) * kD;
+    const int64_t page = slot / a.page_size, off = slot % a.page_size;
+    const __nv_bfloat16* row = a.qkv + static_cast<int64_t>(t) * a.ld_qkv;
+
+    for (int h0 = warp; h0 < heads; h0 += kRopeWarps * kHeadsPerPass) {
+        uint32_t lo[kHeadsPerPass], hi[kHeadsPerPass];
+#pragma unroll
+        for (int j = 0; j < kHeadsPerPass; ++j) {
+            const int h = h0 + j * kRopeWarps;
+            if (h < heads) {
+                lo[j] = ld_b32(row + static_cast<int64_t>(h) * kD + i0);
+                hi[j] = ld_b32(row + static_cast<int64_t>(h) * kD + kHalf + i0);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kHeadsPerPass; ++j) {
+            const int h = h0 + j * kRopeWarps;  // the same for every lane
+            if (h >= heads) break;
+            if (h >= a.Hq + a.Hkv) {  // v: copy into the cache
+                const int hv = h - a.Hq - a.Hkv;
+                __nv_bfloat16* dst = a.v_cache + ((page * a.Hkv + hv) * a.page_size + off) * kD;
+                *reinterpret_cast<uint32_t*>(dst + i0) = lo[j];
+                *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = hi[j];
+                continue;
+            }
+            float x[4] = {__uint_as_float(lo[j] << 16), __uint_as_float(lo[j] & 0xffff0000u),
+                          __uint_as_float(hi[j] << 16), __uint_as_float(hi[j] & 0xffff0000u)};
+            const bool is_q = h < a.Hq;
+            if (is_q ? a.q_norm_w != nullptr : a.k_norm_w != nullptr) {
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ss = __fmaf_rn(x[e], x[e], ss);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float r = rsqrtf(__fdiv_rn(ss, static_cast<float>(kD)) + a.eps);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    x[e] = __bfloat162float(
+                        __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[e], r), is_q ? qw[e] : kw[e])));
+            }
+            float y[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                y[e] = __fsub_rn(__fmul_rn(x[e], c[e]), __fmul_rn(x[2 + e], sn[e]));
+                y[2 + e] = __fadd_rn(__fmul_rn(x[2 + e], c[e]), __fmul_rn(x[e], sn[e]));
+            }
+            __nv_bfloat16* dst;
+            if (is_q) {
+                dst = a.q_out + (static_cast<int64_t>(t) * a.Hq + h) * kD;
+            } else {
+                dst = a.k_cache + ((page * a.Hkv + (h - a.Hq)) * a.page_size + off) * kD;
+            }
+            *reinterpret_cast<uint32_t*>(dst + i0) = bi::pack_bf16x2(y[0], y[1]);
+            *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = bi::pack_bf16x2(y[2], y[3]);
+        }
     }
-    *reinterpret_cast<__nv_bfloat162*>(dst + i0) = __floats2bfloat162_rn(y[0], y[1]);
-    *reinterpret_cast<__nv_bfloat162*>(dst + kHalf + i0) = __floats2bfloat162_rn(y[2], y[3]);
 }
 
 // h[t][j] = bf16( silu(g) * u ),  g = gu[t][j], u = gu[t][F + j],
@@ -177,10 +206,7 @@ extern "C" bi_status bi_qk_norm_rope_append(const void* qkv, int64_t ld_qkv, int
     a.num_slots = static_cast<int64_t>(num_pages) * page_size;
     a.page_size = page_size;
     a.err = bi::device_error_word();
-    const int64_t warps = static_cast<int64_t>(T) * (Hq + 2 * Hkv);
-    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (blocks > 0x7fffffffLL) return BI_ERR_UNSUPPORTED_SHAPE;
-    qk_norm_rope_append_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+    qk_norm_rope_append_kernel<<<static_cast<unsigned>(T), kRopeWarps * 32, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 

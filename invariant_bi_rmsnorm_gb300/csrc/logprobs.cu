@@ -8,11 +8,16 @@
 // reduction over the vocabulary, so it gets the same treatment as RMSNorm:
 // one row per CTA and an order that depends only on the row length.
 //
-//   pass 1:  m = max_j x_j                      (exact, order-free)
-//   pass 2:  s = sum_j exp(x_j - m) in fp32:    thread t adds its 16-byte
-//            vectors t, t+256, ... in order, each left to right; then an xor
-//            butterfly over the warp; then the 8 warp sums in warp order
-//   lse = m + log(s);   logprob = x_target - lse
+// One pass over the row (read once from HBM).  Thread t owns the 16-byte
+// vectors t, t+256, t+512, ... and folds them in that order into a running
+// (m, s) pair with sum_j exp(x_j - m) = s, exponentials taken base 2 with
+// c = log2(e) rounded to fp32 and mc = fp32(m * c):
+//     m' = max(m, max of the vector's 8 values);  s = s * 2^((m - m') c);
+//     s += 2^(fma(x_e, c, -mc')) for e = 0..7 in element order     (fp32)
+// Then an xor butterfly over the warp and the 8 warp pairs in warp order,
+// each step  M = max(m1, m2);  s = s1 2^((m1 - M) c) + s2 2^((m2 - M) c).
+//   lse = M + log(s);   logprob = x_target - lse
+// Every step depends only on the vocabulary size, never on the row count.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -27,49 +32,76 @@ constexpr int kThreads = 256;
 __device__ __forceinline__ float lo16(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float hi16(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+// exp(a - b) for a <= b, as 2^((a - b) c); 0 when a is -inf
+__device__ __forceinline__ float rescale(float a, float b) {
+    return exp2f(__fmul_rn(__fsub_rn(a, b), kLog2e));
+}
+
+// (m, s) after folding one vector of 8 values in element order; mc = m * c
+__device__ __forceinline__ void fold_vec(float& m, float& mc, float& s, const uint4& u) {
+    const float x[8] = {lo16(u.x), hi16(u.x), lo16(u.y), hi16(u.y),
+                        lo16(u.z), hi16(u.z), lo16(u.w), hi16(u.w)};
+    float vm = x[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e) vm = fmaxf(vm, x[e]);
+    if (vm == -INFINITY) return;  // nothing visible in this vector
+    if (vm > m) {
+        s = __fmul_rn(s, rescale(m, vm));  // m = -inf: s is 0 and stays 0
+        m = vm;
+        mc = __fmul_rn(vm, kLog2e);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s = __fadd_rn(s, exp2f(__fmaf_rn(x[e], kLog2e, -mc)));
+}
+
+// (m1, s1) <- (m1, s1) combined with (m2, s2); symmetric in its operands
+__device__ __forceinline__ void combine(float& m1, float& s1, float m2, float s2) {
+    const float M = fmaxf(m1, m2);
+    if (M == -INFINITY) return;  // both empty
+    s1 = __fadd_rn(__fmul_rn(s1, rescale(m1, M)), __fmul_rn(s2, rescale(m2, M)));
+    m1 = M;
+}
+
+constexpr int kUnroll = 4;
+
 __global__ void __launch_bounds__(kThreads)
     logprobs_kernel(const __nv_bfloat16* __restrict__ logits, int64_t ld, int vocab,
                     const int32_t* __restrict__ targets, float* __restrict__ logprob_out,
                     float* __restrict__ lse_out, uint32_t* err) {
-    __shared__ float red[kThreads / 32];
+    __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
     const __nv_bfloat16* x = logits + row * ld;
     const uint4* xv = reinterpret_cast<const uint4*>(x);
     const int nvec = vocab / 8;
 
-    float m = -INFINITY;
-    for (int v = tid; v < nvec; v += kThreads) {
-        const uint4 u = xv[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float m = -INFINITY, mc = -INFINITY, s = 0.f;
+    int v = tid;
+    // kUnroll vectors in flight per thread; folded in ascending order
+    for (; v + (kUnroll - 1) * kThreads < nvec; v += kUnroll * kThreads) {
+        uint4 u[kUnroll];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(lo16(w[e]), hi16(w[e])));
+        for (int i = 0; i < kUnroll; ++i) u[i] = __ldcs(xv + v + i * kThreads);
+#pragma unroll
+        for (int i = 0; i < kUnroll; ++i) fold_vec(m, mc, s, u[i]);
     }
+    for (; v < nvec; v += kThreads) fold_vec(m, mc, s, __ldcs(xv + v));
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((tid & 31) == 0) red[tid >> 5] = m;
-    __syncthreads();
-    float M = red[0];
-    for (int i = 1; i < kThreads / 32; ++i) M = fmaxf(M, red[i]);
-    __syncthreads();
-
-    float s = 0.f;
-    for (int v = tid; v < nvec; v += kThreads) {
-        const uint4 u = xv[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            s = __fadd_rn(s, expf(__fsub_rn(lo16(w[e]), M)));
-            s = __fadd_rn(s, expf(__fsub_rn(hi16(w[e]), M)));
-        }
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        combine(m, s, m2, s2);
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((tid & 31) == 0) red[tid >> 5] = s;
+    if ((tid & 31) == 0) {
+        red_m[tid >> 5] = m;
+        red_s[tid >> 5] = s;
+    }
     __syncthreads();
     if (tid != 0) return;
-    float S = red[0];
-    for (int i = 1; i < kThreads / 32; ++i) S = __fadd_rn(S, red[i]);
+    float M = red_m[0], S = red_s[0];
+    for (int i = 1; i < kThreads / 32; ++i) combine(M, S, red_m[i], red_s[i]);
     const float lse = __fadd_rn(M, logf(S));
     if (lse_out) lse_out[row] = lse;
     if (targets && logprob_out) {

@@ -65,7 +65,10 @@ __device__ __forceinline__ void consumer_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads)
+#ifndef BI_PREFILL_MIN_BLOCKS
+#define BI_PREFILL_MIN_BLOCKS 2
+#endif
+__global__ void __launch_bounds__(kThreads, BI_PREFILL_MIN_BLOCKS)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
     const int tile = blockIdx.x;

@@ -41,3 +41,30 @@ def test_bad_target_reported_without_fault():
     with pytest.raises(bi.BiError, match="BAD_INPUT"):
         bi.get_device_error()
     assert torch.isnan(lp[1]) and not torch.isnan(lp[0])
+
+
+def test_masked_vocabulary_entries():
+    """-inf logits (a masked vocabulary) contribute nothing: rows with 90% of
+    entries masked, a row with one visible entry (lse = that entry, its
+    log-probability 0, up to fp32 rounding), and a row masked except its last
+    vector."""
+    x = inputs.normal_bf16((6, V), seed=94, std=3.0)
+    g = torch.Generator().manual_seed(95)
+    mask = torch.rand((6, V), generator=g) < 0.9
+    x[mask] = float("-inf")
+    x[3] = float("-inf")
+    x[3, 77777] = 1.5
+    x[4, :V - 8] = float("-inf")
+    x[5, :1000] = float("-inf")
+    t = torch.tensor([int(torch.nonzero(~mask[0])[0]), int(torch.nonzero(~mask[1])[0]),
+                      int(torch.nonzero(~mask[2])[0]), 77777, V - 3,
+                      1000 + int(torch.nonzero(~mask[5, 1000:])[0])], dtype=torch.int32)
+    xd, td = x.cuda(), t.cuda()
+    lp, lse = bi.logprobs(xd, td)
+    lp_ref, lse_ref = oracle.logprobs(x, t.numpy())
+    for got, ref in ((lp, lp_ref), (lse, lse_ref)):
+        g_ = got.cpu().double().numpy()
+        assert np.isfinite(g_).all()
+        assert (np.abs(g_ - ref) <= 1e-4 + 1e-6 * np.abs(ref)).all(), np.abs(g_ - ref).max()
+    assert abs(lse[3].item() - 1.5) <= 1e-6 and abs(lp[3].item()) <= 1e-6
+    bi.get_device_error()
