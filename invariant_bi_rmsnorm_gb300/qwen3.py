@@ -142,26 +142,49 @@ class Engine:
         seq.pages = []
 
     # ---------------------------------------------------------- forward ----
-    def forward(self, items, want_logits):
+    def forward(self, items, want_logits, pending=None):
         """One step.  items: list of (seq, n) -- process the next n uncached
         tokens of seq.  want_logits: per item, whether its last token's logits
-        are needed.  Returns logits [sum(want_logits), vocab] (bf16)."""
+        are needed.  pending: None, or (picks, {id(seq): j}) for decode items
+        whose input token is the previous step's pick still on the device
+        (picks[j]).  Returns logits [sum(want_logits), vocab] (bf16) or None.
+        Nothing here waits for the device: step metadata goes up from pinned
+        host memory behind the work already queued."""
         cfg = self.cfg
+        dev = self.device
         toks, pos, slots = [], [], []
+        fill_rows, fill_src = [], []
+        src_of = pending[1] if pending is not None else {}
         for seq, n in items:
             t0 = seq.n_cached
             self._ensure_pages(seq, t0 + n)
-            all_t = seq.tokens
-            for t in range(t0, t0 + n):
-                toks.append(all_t[t])
-                pos.append(t)
-                slots.append(seq.pages[t // PAGE_SIZE] * PAGE_SIZE + t % PAGE_SIZE)
+            if n == 1:
+                j = src_of.get(id(seq))
+                if j is not None:
+                    fill_rows.append(len(toks))
+                    fill_src.append(j)
+                    toks.append(0)
+                else:
+                    toks.append(seq.tokens[t0])
+                pos.append(t0)
+                slots.append(seq.pages[t0 // PAGE_SIZE] * PAGE_SIZE + t0 % PAGE_SIZE)
+            else:
+                tt = np.arange(t0, t0 + n)
+                toks.extend(seq.tokens[t0:t0 + n])
+                pos.extend(range(t0, t0 + n))
+                slots.extend((np.asarray(seq.pages)[tt // PAGE_SIZE] * PAGE_SIZE
+                              + tt % PAGE_SIZE).tolist())
         T = len(toks)
         if T > self.budget:
             raise ValueError("step exceeds the token budget")
-        dev = self.device
-        i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32)).to(dev, non_blocking=True)  # noqa: E731
-        tok_d = torch.as_tensor(np.asarray(toks, dtype=np.int64)).to(dev)
+
+        def up(a, dtype):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=dtype)).pin_memory().to(
+                dev, non_blocking=True)
+        i32 = lambda a: up(a, np.int32)  # noqa: E731
+        tok_d = up(toks, np.int64)
+        if fill_rows:
+            tok_d[up(fill_rows, np.int64)] = pending[0][up(fill_src, np.int64)]
         pos_d, slot_d = i32(pos), i32(slots)
 
         # decode items (one token) and prompt items, each with its own metadata
@@ -181,8 +204,7 @@ class Engine:
             rows = np.array([offs[k] for k, _, _ in dec], dtype=np.int64)
             lens = [s.n_cached + 1 for _, s, _ in dec]
             bt = table(dec)
-            meta["dec"] = (torch.as_tensor(rows).to(dev), i32(bt), i32(lens), int(max(lens)),
-                           bt.shape[1])
+            meta["dec"] = (self._rows(rows, up), i32(bt), i32(lens), int(max(lens)), bt.shape[1])
         if pre:
             starts = [int(offs[k]) for k, _, _ in pre]
             nqs = [n for _, _, n in pre]
@@ -191,7 +213,7 @@ class Engine:
             indptr = np.concatenate([[0], np.cumsum(nqs)])
             lens = [s.n_cached + n for _, s, n in pre]
             bt = table(pre)
-            meta["pre"] = (torch.as_tensor(rows).to(dev), i32(bt), i32(lens), i32(indptr),
+            meta["pre"] = (self._rows(rows, up), i32(bt), i32(lens), i32(indptr),
                            int(max(nqs)), int(max(lens)))
 
         b = {k: v[:T] for k, v in self.buf.items()}
@@ -219,7 +241,7 @@ class Engine:
         samp = [int(offs[k + 1] - 1) for k, want in enumerate(want_logits) if want]
         if not samp:
             return None
-        nrows = torch.index_select(b["n"], 0, torch.as_tensor(samp, dtype=torch.int64).to(dev))
+        nrows = torch.index_select(b["n"], 0, up(samp, np.int64))
         self.steps += 1
         return gemm(nrows, self.w.lm_head, out=torch.empty(len(samp), cfg.vocab,
                                                            dtype=torch.bfloat16, device=dev))
@@ -242,31 +264,52 @@ class Engine:
             return out
         return t_gemm, t_rmsnorm, t_add_rmsnorm
 
+    @staticmethod
+    def _rows(rows, up):
+        """A group's token rows: a slice when they are one contiguous run (the
+        scheduler puts decode rows first and prompt rows after them), else a
+        device index tensor."""
+        if len(rows) and rows[-1] - rows[0] + 1 == len(rows) and (np.diff(rows) == 1).all():
+            return slice(int(rows[0]), int(rows[-1]) + 1)
+        return up(rows, np.int64)
+
     def _attention(self, l, b, meta):
-        cfg = self.cfg
         kc, vc = self.k_cache[l], self.v_cache[l]
-        if "dec" in meta:
-            rows, bt, lens, mx, _ = meta["dec"]
-            q = torch.index_select(b["q"], 0, rows)
-            out = decode_attention(q, kc, vc, bt, lens, max_seq_len=mx)
-            b["attn"].index_copy_(0, rows, out)
-        if "pre" in meta:
-            rows, bt, lens, indptr, mq, mx = meta["pre"]
-            q = torch.index_select(b["q"], 0, rows)
-            out = prefill_attention(q, kc, vc, bt, lens, indptr, max_q_len=mq, max_seq_len=mx)
-            b["attn"].index_copy_(0, rows, out)
+        for kind in ("dec", "pre"):
+            if kind not in meta:
+                continue
+            rows = meta[kind][0]
+            if isinstance(rows, slice):  # q rows and outputs in place
+                q, out = b["q"][rows], b["attn"][rows]
+            else:
+                q, out = torch.index_select(b["q"], 0, rows), None
+            if kind == "dec":
+                _, bt, lens, mx, _ = meta[kind]
+                out = decode_attention(q, kc, vc, bt, lens, max_seq_len=mx, out=out)
+            else:
+                _, bt, lens, indptr, mq, mx = meta[kind]
+                out = prefill_attention(q, kc, vc, bt, lens, indptr, max_q_len=mq,
+                                        max_seq_len=mx, out=out)
+            if not isinstance(rows, slice):
+                b["attn"].index_copy_(0, rows, out)
 
     # ------------------------------------------------------- scheduling ----
     def generate(self, seqs: list[Sequence], record: set | None = None):
         """Run every sequence to max_new generated tokens.  Returns
         {sid: [logits row per generated token]} (CPU bf16) for sids in `record`;
         the log-probability of each generated token (bi_logprobs, fp32) goes to
-        self.logprobs[sid] for the same sids."""
+        self.logprobs[sid] for the same sids.
+
+        The host runs one step ahead of the device: step i+1 is planned and
+        queued while step i computes (no request ends early, so the schedule
+        never needs a token's value), its decode rows take their input tokens
+        straight from step i's picks on the device, and step i's picks are
+        read back only after step i+1 has been queued."""
         record = record or set()
-        logs = {sid: [] for sid in record}
-        self.logprobs = {sid: [] for sid in record}
+        rec_rows = {sid: [] for sid in record}  # device rows, copied to the host at the end
         waiting = deque(seqs)
         running: list[Sequence] = []
+        prev = None
         while waiting or running:
             items, budget = [], self.budget
             for s in running:
@@ -283,32 +326,61 @@ class Engine:
                 else:
                     break
             want = [s.n_cached + n == len(s.tokens) for s, n in items]
-            logits = self.forward(items, want)
-            chosen = []
-            if logits is not None:
-                nxt = torch.argmax(logits, dim=-1).cpu().tolist()
-                sampled = [s for (s, n), w in zip(items, want) if w]
-                chosen = [s.forced[len(s.generated)] if s.forced is not None else nxt[j]
-                          for j, s in enumerate(sampled)]
-                if record:
-                    tgt = torch.as_tensor(np.asarray(chosen, dtype=np.int32)).to(self.device)
-                    lps, _ = logprobs(logits, tgt)
-                    lps = lps.cpu()
-            j = 0
-            for (s, n), w in zip(items, want):
+            logits = self.forward(items, want, pending=prev[:2] if prev else None)
+            if prev is not None:
+                self._resolve(prev)
+            prev = None
+            for s, n in items:
                 s.n_cached += n
-                if not w:
-                    continue
-                if s.sid in record:
-                    logs[s.sid].append(logits[j].cpu())
-                    self.logprobs[s.sid].append(lps[j].clone())
-                s.generated.append(int(chosen[j]))
-                j += 1
+            sampled = [s for (s, n), w in zip(items, want) if w]
+            if logits is not None:
+                picks = torch.argmax(logits, dim=-1)
+                forced = [(j, s.forced[len(s.generated)]) for j, s in enumerate(sampled)
+                          if s.forced is not None]
+                if forced:
+                    fj = torch.tensor([j for j, _ in forced], dtype=torch.int64, device=self.device)
+                    fv = torch.tensor([v for _, v in forced], dtype=torch.int64, device=self.device)
+                    picks[fj] = fv
+                rec = [(j, s.sid) for j, s in enumerate(sampled) if s.sid in record]
+                if rec:
+                    rj = torch.tensor([j for j, _ in rec], dtype=torch.int64, device=self.device)
+                    lg = torch.index_select(logits, 0, rj)
+                    lps, _ = logprobs(lg, picks[rj].to(torch.int32))
+                    for i, (_, sid) in enumerate(rec):
+                        rec_rows[sid].append((lg, lps, i))
+                host = torch.empty(picks.shape, dtype=picks.dtype, pin_memory=True)
+                host.copy_(picks, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record()
+                slot_of = {}
+                for j, s in enumerate(sampled):
+                    slot_of[id(s)] = j
+                    s.generated.append(None)  # filled in by _resolve
+                prev = (picks, slot_of, host, ev, sampled)
             running = [s for s in running + admitted if not s.done]
             for s in seqs:
                 if s.done and s.pages:
                     self._release(s)
+        if prev is not None:
+            self._resolve(prev)
+        logs, self.logprobs = {}, {}
+        for sid, rows in rec_rows.items():
+            lg = torch.stack([t[i] for t, _, i in rows]).cpu() if rows else None
+            lp = torch.stack([t[i] for _, t, i in rows]).cpu() if rows else None
+            logs[sid] = list(lg.unbind(0)) if rows else []
+            self.logprobs[sid] = list(lp.unbind(0)) if rows else []
         return logs
+
+    @staticmethod
+    def _resolve(prev):
+        """Wait for one step's picks to reach the host and store them."""
+        _, _, host, ev, sampled = prev
+        ev.synchronize()
+        vals = host.tolist()
+        for j, s in enumerate(sampled):
+            # a step is resolved before the next one appends its placeholder,
+            # so the step's pick is the last entry
+            s.generated[-1] = int(vals[j])
 
     def reset(self):
         self.free_pages = deque(range(self.num_pages))
