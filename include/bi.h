@@ -132,6 +132,32 @@ bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, int32_t N, i
                   int64_t ld_x, int64_t ld_w, int64_t ld_y, cudaStream_t stream);
 
 /*
+ * bi_gemm_swiglu -- the gate|up projection of a SwiGLU MLP fused with the
+ * SwiGLU product:
+ *     h[M][F] = bf16( silu(g) * u ),  g = bf16((x . W_gate^T)[m][j]),
+ *                                     u = bf16((x . W_up^T)[m][j])
+ * with silu(g) = g / (1 + exp(-g)) in fp32 -- bit-identical to bi_gemm into a
+ * [M][2F] buffer followed by bi_silu_mul, without writing that buffer.
+ *
+ * Operation: bi_gemm's main loop (same tile, instruction shape and K order,
+ * so the same batch invariance) with a pointwise epilogue ("Achieving
+ * Batch-Invariant Kernels": pointwise operations are batch-invariant).  The
+ * pages do not fuse it; this is a layout choice for the decoder's MLP.
+ *
+ *   x     device, bf16 [M][ld_x], as bi_gemm.
+ *   W_gu  device, bf16 [2F][ld_w]: the gate and up weights (nn.Linear layout)
+ *         with rows interleaved in groups of 8 -- rows 16i .. 16i+7 are gate
+ *         rows 8i .. 8i+7 and rows 16i+8 .. 16i+15 are up rows 8i .. 8i+7.
+ *   h     device, bf16 [M][ld_h]; must not overlap x or W_gu.
+ *   M  0 .. 2^31-257;  F >= 8 and a multiple of 8;  K >= 8, multiple of 8.
+ *   ld_x, ld_w, ld_h  in elements, multiples of 8, >= K, >= K, >= F.
+ * Pointers must be 16-byte aligned.  Errors as bi_gemm.
+ */
+bi_status bi_gemm_swiglu(const void* x, const void* W_gu, void* h, int32_t M, int32_t F,
+                         int32_t K, int64_t ld_x, int64_t ld_w, int64_t ld_h,
+                         cudaStream_t stream);
+
+/*
  * Workspace bytes bi_decode_attention needs for B sequences of at most
  * max_seq_len tokens with Hq query heads of size D: one fp32 partial
  * (max, sum, D-vector) per (sequence, query head, 256-token chunk).

@@ -215,6 +215,43 @@ def gemm(x: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None,
     return out
 
 
+def interleave_gate_up(W_gate_up: torch.Tensor) -> torch.Tensor:
+    """[2F, K] weight with the gate rows first and the up rows after them ->
+    the [2F, K] layout bi_gemm_swiglu reads: groups of 8 gate rows, each
+    followed by the 8 matching up rows."""
+    F2, K = W_gate_up.shape
+    if F2 % 16:
+        raise ValueError("interleave_gate_up: 2F must be a multiple of 16")
+    F = F2 // 2
+    g = W_gate_up[:F].reshape(F // 8, 8, K)
+    u = W_gate_up[F:].reshape(F // 8, 8, K)
+    return torch.cat([g, u], dim=1).reshape(F2, K).contiguous()
+
+
+def gemm_swiglu(x: torch.Tensor, W_gu: torch.Tensor, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Batch-invariant h = silu(x @ W_gate.T) * (x @ W_up.T), bit-identical to
+    silu_mul(gemm(x, W_gate_up)); W_gu is interleave_gate_up(W_gate_up)."""
+    _cuda_bf16(x, "x")
+    _cuda_bf16(W_gu, "W_gu")
+    if x.dim() != 2 or W_gu.dim() != 2 or x.shape[1] != W_gu.shape[1]:
+        raise ValueError("gemm_swiglu: x [M, K] and W_gu [2F, K] expected")
+    M, K = x.shape
+    if W_gu.shape[0] % 16:
+        raise ValueError("gemm_swiglu: W_gu must have 2F rows, F a multiple of 8")
+    F = W_gu.shape[0] // 2
+    if out is None:
+        out = torch.empty((M, F), dtype=torch.bfloat16, device=x.device)
+    _cuda_bf16(out, "out")
+    if tuple(out.shape) != (M, F):
+        raise ValueError("gemm_swiglu: out has the wrong shape")
+    _check(_lib.load().bi_gemm_swiglu(x.data_ptr(), W_gu.data_ptr(), out.data_ptr(), M, F, K,
+                                      _row_major_2d(x, "x"), _row_major_2d(W_gu, "W_gu"),
+                                      _row_major_2d(out, "out"), _stream(stream)),
+           "bi_gemm_swiglu")
+    return out
+
+
 # ----------------------------------------------------------- attention ------
 def decode_attention_workspace_size(B: int, Hq: int, D: int, max_seq_len: int) -> int:
     return int(_lib.load().bi_decode_attention_workspace_size(B, Hq, D, max_seq_len))

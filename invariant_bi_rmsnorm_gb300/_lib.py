@@ -30,6 +30,7 @@ EXPORTS = (
     "bi_decode_attention", "bi_decode_attention_noalloc", "bi_decode_attention_fixed_splits",
     "bi_selftest_wait_timeout", "bi_prefill_attention", "bi_add_rmsnorm",
     "bi_qk_norm_rope_append", "bi_silu_mul", "bi_decode_attention_launches", "bi_logprobs",
+    "bi_gemm_swiglu",
 )
 
 _lib = None
@@ -59,6 +60,8 @@ def load() -> ctypes.CDLL:
     lib.bi_rmsnorm.restype = ctypes.c_int
     lib.bi_gemm.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i64, _i64, _i64, _vp]
     lib.bi_gemm.restype = ctypes.c_int
+    lib.bi_gemm_swiglu.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i64, _i64, _i64, _vp]
+    lib.bi_gemm_swiglu.restype = ctypes.c_int
     lib.bi_decode_attention_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
     lib.bi_decode_attention_workspace_size.restype = ctypes.c_size_t
     lib.bi_decode_num_chunks.argtypes = [_i32]

@@ -276,4 +276,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// SwiGLU of one bf16 pair, in fp32: silu(g) * u with silu(g) = g / (1 + exp(-g)).
+// The one definition both bi_silu_mul and the fused GEMM epilogue use, so the
+// two give the same bits.
+__device__ __forceinline__ float swiglu(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.f, expf(-g))), u);
+}
+
 }  // namespace bi

@@ -169,10 +169,8 @@ __global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float ga = __low2float(g2[e]), gb = __high2float(g2[e]);
-            const float sa = __fdiv_rn(ga, __fadd_rn(1.f, expf(-ga)));
-            const float sb = __fdiv_rn(gb, __fadd_rn(1.f, expf(-gb)));
-            o[e] = bi::pack_bf16x2(__fmul_rn(sa, __low2float(u2[e])), __fmul_rn(sb, __high2float(u2[e])));
+            o[e] = bi::pack_bf16x2(bi::swiglu(__low2float(g2[e]), __low2float(u2[e])),
+                                   bi::swiglu(__high2float(g2[e]), __high2float(u2[e])));
         }
         *reinterpret_cast<uint4*>(out + t * ld_out + j) = make_uint4(o[0], o[1], o[2], o[3]);
     }

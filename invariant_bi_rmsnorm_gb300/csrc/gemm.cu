@@ -22,6 +22,11 @@
 //   warps 2..5  epilogue in each CTA: tcgen05.ld of its own 128 rows of the
 //               accumulator (warp w reads TMEM lanes 32*(w%4) ..), fp32 -> bf16
 //               round-to-nearest-even, store.
+// The fused SwiGLU variant (bi_gemm_swiglu) runs the same main loop over a
+// gate|up weight whose rows are interleaved in groups of 8 (8 gate rows, then
+// the 8 matching up rows); its epilogue rounds each gate and up value to bf16
+// exactly as the plain GEMM would store them, then writes
+// bf16(silu(gate) * up) -- the bits bi_gemm followed by bi_silu_mul give.
 // Rows past M and columns past N read as zeros (TMA out-of-bounds fill) and
 // are never stored; adding zero products leaves the other sums unchanged.
 #include <cuda_bf16.h>
@@ -82,6 +87,11 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(BMP >> 4) << 24);
 }  // namespace pair
 
+__device__ __forceinline__ float round_bf16(uint32_t acc_bits) {
+    return __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc_bits)));
+}
+
+template <bool kSwiGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmap_x,
                              const __grid_constant__ CUtensorMap tmap_w,
@@ -227,7 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                 uint32_t r[32];
                 bi::tmem_ld_32x32b_x32(taddr + ch * 32, r);
                 bi::tmem_ld_wait();
-                if (row < M) {
+                if (row < M && !kSwiGLU) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         if (col0 + 8 * v + 8 > N) break;
@@ -237,6 +247,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                         o.z = bi::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
                         o.w = bi::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
                         *reinterpret_cast<uint4*>(yrow + col0 + 8 * v) = o;
+                    }
+                } else if (row < M) {
+                    // two groups of 16 accumulator columns: 8 gate, then 8 up
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        if (col0 + 16 * v + 16 > N) break;
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float h0 = bi::swiglu(round_bf16(r[16 * v + 2 * e]),
+                                                        round_bf16(r[16 * v + 8 + 2 * e]));
+                            const float h1 = bi::swiglu(round_bf16(r[16 * v + 2 * e + 1]),
+                                                        round_bf16(r[16 * v + 8 + 2 * e + 1]));
+                            o[e] = bi::pack_bf16x2(h0, h1);
+                        }
+                        *reinterpret_cast<uint4*>(yrow + (col0 + 16 * v) / 2) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
             }
@@ -258,17 +285,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     }
 }
 
-bool g_attr_set[64] = {};
+bool g_attr_set[2][64] = {};
 
-}  // namespace
-
-extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, int32_t N,
-                             int32_t K, int64_t ld_x, int64_t ld_w, int64_t ld_y,
-                             cudaStream_t stream) {
+// Validate and launch.  N is the weight's row count (the accumulator width);
+// the output has N columns, or N/2 for the fused SwiGLU variant.
+template <bool kSwiGLU>
+bi_status launch_gemm(const void* x, const void* W, void* y, int32_t M, int32_t N, int32_t K,
+                      int64_t ld_x, int64_t ld_w, int64_t ld_y, cudaStream_t stream) {
+    const int64_t out_cols = kSwiGLU ? N / 2 : N;
     if (M < 0 || N < 8 || K < 8) return M < 0 ? BI_ERR_INVALID_ARG : BI_ERR_UNSUPPORTED_SHAPE;
     if (M > 0x7fffffff - pair::BMP) return BI_ERR_UNSUPPORTED_SHAPE;  // row indices stay in int
-    if ((N & 7) || (K & 7)) return BI_ERR_UNSUPPORTED_SHAPE;
-    if (ld_x < K || ld_w < K || ld_y < N) return BI_ERR_INVALID_ARG;
+    if ((N & (kSwiGLU ? 15 : 7)) || (K & 7)) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (ld_x < K || ld_w < K || ld_y < out_cols) return BI_ERR_INVALID_ARG;
     if ((ld_x & 7) || (ld_w & 7) || (ld_y & 7)) return BI_ERR_MISALIGNED;
     if (M == 0) return BI_OK;
     if (!x || !W || !y) return BI_ERR_INVALID_ARG;
@@ -283,13 +311,13 @@ extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, i
         return BI_ERR_CUDA;
 
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BI_ERR_CUDA;
-    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_tcgen05_pair_kernel,
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
+    if (!g_attr_set[kSwiGLU][dev]) {
+        if (cudaFuncSetAttribute(gemm_tcgen05_pair_kernel<kSwiGLU>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  pair::kSmemBytes) != cudaSuccess)
             return BI_ERR_CUDA;
-        g_attr_set[dev] = true;
+        g_attr_set[kSwiGLU][dev] = true;
     }
     const int sms = bi::sm_count();
     if (sms < 2) return BI_ERR_CUDA;
@@ -303,7 +331,22 @@ extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, i
     const int64_t budget = int64_t{64} << 20;
     int group_m = num_m;
     if (slab * num_m > budget) group_m = static_cast<int>(std::max<int64_t>(1, budget / slab));
-    gemm_tcgen05_pair_kernel<<<2 * pairs, pair::kThreads, pair::kSmemBytes, stream>>>(
+    gemm_tcgen05_pair_kernel<kSwiGLU><<<2 * pairs, pair::kThreads, pair::kSmemBytes, stream>>>(
         tx, tw, static_cast<__nv_bfloat16*>(y), M, N, K, ld_y, group_m, bi::device_error_word());
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" bi_status bi_gemm(const void* x, const void* W, void* y, int32_t M, int32_t N,
+                             int32_t K, int64_t ld_x, int64_t ld_w, int64_t ld_y,
+                             cudaStream_t stream) {
+    return launch_gemm<false>(x, W, y, M, N, K, ld_x, ld_w, ld_y, stream);
+}
+
+extern "C" bi_status bi_gemm_swiglu(const void* x, const void* W_gu, void* h, int32_t M,
+                                    int32_t F, int32_t K, int64_t ld_x, int64_t ld_w,
+                                    int64_t ld_h, cudaStream_t stream) {
+    if (F < 8 || F > (0x7fffffff >> 1)) return BI_ERR_UNSUPPORTED_SHAPE;
+    return launch_gemm<true>(x, W_gu, h, M, 2 * F, K, ld_x, ld_w, ld_h, stream);
 }

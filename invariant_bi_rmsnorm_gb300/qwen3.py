@@ -25,8 +25,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import (add_rmsnorm, decode_attention, gemm, logprobs, prefill_attention,
-               qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
+from . import (add_rmsnorm, decode_attention, gemm, gemm_swiglu, interleave_gate_up, logprobs,
+               prefill_attention, qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
 from . import inputs
 from ._lib import PAGE_SIZE
 
@@ -127,6 +127,10 @@ class Engine:
         self.buf = {"res": e(T, H), "n": e(T, H), "qkv": e(T, (cfg.heads + 2 * Hkv) * D),
                     "q": e(T, cfg.heads, D), "attn": e(T, cfg.heads, D), "o": e(T, H),
                     "gu": e(T, 2 * F), "h": e(T, F), "d": e(T, H)}
+        # the bi path runs gate|up and SwiGLU as one fused GEMM over an
+        # interleaved copy of the weight (bit-identical to gemm + silu_mul)
+        self.gate_up_il = ([interleave_gate_up(self.w.layers[l]["gate_up"])
+                            for l in range(self.n_layers)] if ops == "bi" else None)
         self.steps = 0
 
     # ------------------------------------------------------------ pages ----
@@ -234,8 +238,11 @@ class Engine:
             self._attention(l, b, meta)
             gemm(b["attn"].view(T, Hq * cfg.head_dim), L["o"], out=b["o"])
             add_rmsnorm(b["o"], res, L["post_norm"], cfg.eps, out=b["n"])
-            gemm(b["n"], L["gate_up"], out=b["gu"])
-            silu_mul(b["gu"], out=b["h"])
+            if self.gate_up_il is not None:
+                gemm_swiglu(b["n"], self.gate_up_il[l], out=b["h"])
+            else:
+                gemm(b["n"], L["gate_up"], out=b["gu"])
+                silu_mul(b["gu"], out=b["h"])
             gemm(b["h"], L["down"], out=b["d"])
         add_rmsnorm(b["d"], res, self.w.final_norm, cfg.eps, out=b["n"])
         samp = [int(offs[k + 1] - 1) for k, want in enumerate(want_logits) if want]

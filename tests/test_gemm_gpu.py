@@ -116,3 +116,44 @@ def test_c3_rows_invariant_across_m_and_sampled_parity(name):
     assert err.max() <= 1e-2 * np.abs(ref).max()
     absdot = oracle.gemm_entries(pool.abs(), W.abs(), ms, ns)
     assert (err <= 2.0 ** -8 * np.abs(ref) + K * 2.0 ** -22 * absdot + 1e-30).all()
+
+
+# ------------------------------- fused gate|up GEMM + SwiGLU (decoder MLP) ---
+@pytest.mark.parametrize("M,F,K", [(1, 12288, 4096), (300, 12288, 4096), (37, 200, 192),
+                                   (513, 8, 64)])
+def test_gemm_swiglu_equals_gemm_then_silu_mul_bitwise(M, F, K):
+    """The fused epilogue rounds gate and up to bf16 as bi_gemm stores them and
+    applies bi_silu_mul's arithmetic, so the two paths agree bit for bit --
+    across ragged N tiles (2F = 400 and 16 leave a partial last tile) and M."""
+    W = inputs.gemm_weight(2 * F, K, seed=70).cuda()
+    x = inputs.gemm_rows(M, K, seed=71).cuda()
+    unfused = bi.silu_mul(bi.gemm(x, W))
+    fused = bi.gemm_swiglu(x, bi.interleave_gate_up(W))
+    assert torch.equal(fused, unfused)
+    bi.get_device_error()
+
+
+def test_gemm_swiglu_rows_invariant_and_against_oracle():
+    """Rows alone vs in a batch of 512, bitwise; and the fused result against
+    the oracle's GEMM rounded to bf16 with SwiGLU in fp64."""
+    from oracle import decoder as odec
+    F, K = 200, 256
+    W = inputs.gemm_weight(2 * F, K, seed=72)
+    x = inputs.gemm_rows(512, K, seed=73)
+    Wi = bi.interleave_gate_up(W.cuda())
+    full = bi.gemm_swiglu(x.cuda(), Wi)
+    for r in (0, 255, 511):
+        assert torch.equal(bi.gemm_swiglu(x[r:r + 1].cuda(), Wi)[0], full[r])
+    gu = oracle.bf16_to_f64(oracle.round_bf16(oracle.gemm(x, W)))
+    g, u = gu[:, :F], gu[:, F:]
+    ref = odec.silu_mul(g, u)
+    err = np.abs(f64(full) - ref)
+    # g and u may each sit one bf16 step (<= 2^-7 relative) from the oracle's
+    # rounding of the exact sum (fp32 accumulation can cross a rounding
+    # boundary); propagate that through silu(g) * u, plus the output rounding
+    sig = 1.0 / (1.0 + np.exp(-g))
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    bound = (2.0 ** -8 * np.abs(ref) + np.abs(dsilu * u) * 2.0 ** -7 * np.abs(g)
+             + np.abs(g * sig) * 2.0 ** -7 * np.abs(u) + 1e-30)
+    assert (err <= bound).all(), (err / bound).max()
+    bi.get_device_error()
