@@ -69,7 +69,8 @@ def parse_args():
                     help="skip the cold-L2 timings of the kernels beyond the bench step")
     ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "gemm_layers", "attention",
                                        "rmsnorm", "decoder", "prefill", "add_rmsnorm",
-                                       "logprobs", "qk_norm_rope_append", "silu_mul"],
+                                       "logprobs", "qk_norm_rope_append", "silu_mul",
+                                       "gemm_swiglu"],
                     help="time one kernel of the path alone (for profiling); prints its own line")
     ap.add_argument("--requests", type=int, default=1000, help="--case decoder: requests")
     ap.add_argument("--layers", type=int, default=36, help="--case decoder: decoder layers")
@@ -93,7 +94,8 @@ def load_peaks():
 KERNEL_SOURCES = {"bi_gemm": "gemm.cu", "bi_decode_attention": "decode_attention.cu",
                   "bi_rmsnorm": "rmsnorm.cu", "bi_add_rmsnorm": "rmsnorm.cu",
                   "bi_prefill_attention": "prefill_attention.cu", "bi_logprobs": "logprobs.cu",
-                  "bi_qk_norm_rope_append": "decoder_ops.cu", "bi_silu_mul": "decoder_ops.cu"}
+                  "bi_qk_norm_rope_append": "decoder_ops.cu", "bi_silu_mul": "decoder_ops.cu",
+                  "bi_gemm_swiglu": "gemm.cu"}
 
 
 def kernel_source_sha(src: str) -> str:
@@ -352,14 +354,15 @@ class Workload:
             if unit == "TFLOP/s":
                 entry["frac_of_measured_bf16_burst"] = round(rate / bf16, 4)
                 entry["gbs"] = round(info.pop("bytes") / t / 1e6, 1)
-                entry["bound"] = "tensor (mma.sync m16n8k16, not tcgen05)"
+                entry["bound"] = ("tensor (tcgen05)" if name == "gemm_swiglu"
+                                  else "tensor (mma.sync m16n8k16, not tcgen05)")
             else:
                 entry["frac_of_measured_hbm"] = round(rate / hbm, 4)
                 entry["bound"] = "hbm"
-            entry["traffic"] = traffic_record("bi_" + name if name != "prefill"
-                                              else "bi_prefill_attention")
+            kname = "bi_" + name if name != "prefill" else "bi_prefill_attention"
+            entry["traffic"] = traffic_record(kname)
             entry.update(info)
-            res["bi_" + name if name != "prefill" else "bi_prefill_attention"] = entry
+            res[kname] = entry
             del fn
         torch.cuda.synchronize()
         self.bi.get_device_error()
@@ -814,6 +817,16 @@ def build_next_case(name: str, dev, bi, inputs):
         return fn, float(T * per_tok), "GB/s", {
             "tokens": T, "bytes_per_token": "qkv read, q write, k/v cache write, rope row, "
                                            "position and slot"}
+    if name == "gemm_swiglu":
+        # the decoder MLP's gate|up projection fused with SwiGLU, M = 4096 tokens
+        F, K = 12288, HIDDEN
+        x = inputs.gemm_rows(GEMM_M, K, seed=50 + K, device=dev)
+        W = bi.interleave_gate_up(inputs.gemm_weight(2 * F, K, seed=42, device=dev))
+        h = torch.empty(GEMM_M, F, dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.gemm_swiglu(x, W, out=h)  # noqa: E731
+        return fn, 2.0 * GEMM_M * 2 * F * K, "TFLOP/s", {
+            "M": GEMM_M, "F": F, "K": K,
+            "bytes": float(2 * (GEMM_M * K + 2 * F * K + GEMM_M * F))}
     if name == "silu_mul":
         T, F = OPS_TOKENS, 12288
         gu = inputs.normal_bf16((T, 2 * F), 640, device=dev)
@@ -823,7 +836,8 @@ def build_next_case(name: str, dev, bi, inputs):
     raise ValueError(name)
 
 
-NEXT_CASES = ("prefill", "add_rmsnorm", "logprobs", "qk_norm_rope_append", "silu_mul")
+NEXT_CASES = ("prefill", "add_rmsnorm", "logprobs", "qk_norm_rope_append", "silu_mul",
+              "gemm_swiglu")
 
 
 def time_cold(fn, reps: int, flush: torch.Tensor) -> float:
@@ -863,14 +877,14 @@ def run_case(args):
             for (_, N, K), W, y in zip(LAYERS, Ws, ys):
                 bi.gemm(xs[K], W, out=y)
         work, unit = sum(2.0 * GEMM_M * N * K for _, N, K in LAYERS), "TFLOP/s"
+    elif args.case in NEXT_CASES:
+        fn, work, unit, _ = build_next_case(args.case, dev, bi, inputs)
     elif args.case.startswith("gemm"):
         n, N, K = {"gemm_gate_up": LAYERS[2], "gemm_qkv": LAYERS[0]}[args.case]
         x = inputs.gemm_rows(GEMM_M, K, seed=50 + K, device=dev)
         W = inputs.gemm_weight(N, K, seed=42, device=dev)
         y = torch.empty(GEMM_M, N, dtype=torch.bfloat16, device=dev)
         fn, work, unit = (lambda: bi.gemm(x, W, out=y)), 2.0 * GEMM_M * N * K, "TFLOP/s"
-    elif args.case in NEXT_CASES:
-        fn, work, unit, _ = build_next_case(args.case, dev, bi, inputs)
     elif args.case == "attention":
         B = args.batch
         p = inputs.decode_problem(B, max_len=MAX_LEN, seed=270, device=dev)

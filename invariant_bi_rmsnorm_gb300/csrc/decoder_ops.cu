@@ -42,28 +42,29 @@ struct RopeArgs {
     uint32_t* err;
 };
 
-// One CTA of 8 warps per token.  A warp works on two heads at a time, one
-// per half-warp: lane l of half h holds dims 8(l%16) .. 8(l%16)+7 of its head
-// as one 16-byte vector, so lanes l%16 < 8 hold the first half of the head and
-// lane l%16 + 8 their rotation partners.  Warp w takes head pairs w, w+8, ...
-// and issues the loads of up to kPairsPerPass of them before computing any.
+// One CTA of 8 warps per token; warp w takes heads w, w+8, w+16, ... and
+// issues the loads of up to kHeadsPerPass of them before computing any, so
+// enough bytes are in flight to cover HBM latency.  Per head, lane l holds
+// dims 2l, 2l+1 (first half) and 64+2l, 64+2l+1 (their rotation partners):
 //   q, k heads:  x -> bf16(x * rsqrt(mean(x^2) + eps) * w)   (if a norm weight is given;
-//                    sum of squares: per lane over its 8 dims in order, then an
-//                    xor butterfly over the 16 lanes of the head: 8, 4, 2, 1)
+//                    sum of squares: per lane in the order 2l, 2l+1, 64+2l, 64+2l+1, then
+//                    an xor butterfly over lanes)
 //                -> rotate-half RoPE in fp32: y_i = x_i c_i - x_{64+i} s_i,
 //                   y_{64+i} = x_{64+i} c_i + x_i s_i, rounded once to bf16
 //   v heads:     copied.
 // q goes to q_out; k and v to their token's cache slot.  Each head's
 // arithmetic depends only on its own 128 values, the position and the weights.
 constexpr int kRopeWarps = 8;
-constexpr int kPairsPerPass = 3;
+constexpr int kHeadsPerPass = 6;
+
+__device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
 
 __global__ void __launch_bounds__(kRopeWarps * 32) qk_norm_rope_append_kernel(const RopeArgs a) {
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4;
-    const int sl = lane & 15;
     const int heads = a.Hq + 2 * a.Hkv;
     const int pos = a.positions[t];
     const int64_t slot = a.slots[t];
@@ -71,84 +72,71 @@ __global__ void __launch_bounds__(kRopeWarps * 32) qk_norm_rope_append_kernel(co
         if (threadIdx.x == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereDecoderOps);
         return;
     }
-    const int d0 = 8 * sl;           // this lane's first dim
-    const int i0 = d0 & (kHalf - 1);  // its rotation index
-    const bool first = sl < 8;
+    const int i0 = 2 * lane;
     const float* cs = a.rope + static_cast<int64_t>(pos) * kD;
-    float c[8], sn[8], qw[8], kw[8];
+    const float2 cosv = *reinterpret_cast<const float2*>(cs + i0);
+    const float2 sinv = *reinterpret_cast<const float2*>(cs + kHalf + i0);
+    const float c[2] = {cosv.x, cosv.y}, sn[2] = {sinv.x, sinv.y};
+    const int idx[4] = {i0, i0 + 1, kHalf + i0, kHalf + i0 + 1};
+    float qw[4], kw[4];
 #pragma unroll
-    for (int e = 0; e < 8; e += 4) {
-        const float4 cv = *reinterpret_cast<const float4*>(cs + i0 + e);
-        const float4 sv = *reinterpret_cast<const float4*>(cs + kHalf + i0 + e);
-        c[e] = cv.x, c[e + 1] = cv.y, c[e + 2] = cv.z, c[e + 3] = cv.w;
-        sn[e] = sv.x, sn[e + 1] = sv.y, sn[e + 2] = sv.z, sn[e + 3] = sv.w;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        qw[e] = a.q_norm_w ? bf(a.q_norm_w[d0 + e]) : 0.f;
-        kw[e] = a.k_norm_w ? bf(a.k_norm_w[d0 + e]) : 0.f;
+    for (int e = 0; e < 4; ++e) {
+        qw[e] = a.q_norm_w ? bf(a.q_norm_w[idx[e]]) : 0.f;
+        kw[e] = a.k_norm_w ? bf(a.k_norm_w[idx[e]]) : 0.f;
     }
     const int64_t page = slot / a.page_size, off = slot % a.page_size;
     const __nv_bfloat16* row = a.qkv + static_cast<int64_t>(t) * a.ld_qkv;
-    const int pairs = (heads + 1) / 2;
 
-    for (int p0 = warp; p0 < pairs; p0 += kRopeWarps * kPairsPerPass) {
-        uint4 xv[kPairsPerPass];
+    for (int h0 = warp; h0 < heads; h0 += kRopeWarps * kHeadsPerPass) {
+        uint32_t lo[kHeadsPerPass], hi[kHeadsPerPass];
 #pragma unroll
-        for (int j = 0; j < kPairsPerPass; ++j) {
-            const int h = 2 * (p0 + j * kRopeWarps) + half;
-            xv[j] = h < heads ? *reinterpret_cast<const uint4*>(row + static_cast<int64_t>(h) * kD + d0)
-                              : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < kHeadsPerPass; ++j) {
+            const int h = h0 + j * kRopeWarps;
+            if (h < heads) {
+                lo[j] = ld_b32(row + static_cast<int64_t>(h) * kD + i0);
+                hi[j] = ld_b32(row + static_cast<int64_t>(h) * kD + kHalf + i0);
+            }
         }
 #pragma unroll
-        for (int j = 0; j < kPairsPerPass; ++j) {
-            const int pr = p0 + j * kRopeWarps;  // the same for every lane
-            if (pr >= pairs) break;
-            const int h = 2 * pr + half;  // may differ between the half-warps
-            const bool valid = h < heads;
-            const bool is_v = h >= a.Hq + a.Hkv;
-            const bool is_q = h < a.Hq;
-            const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[2 * e] = __uint_as_float(w[e] << 16);
-                x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        for (int j = 0; j < kHeadsPerPass; ++j) {
+            const int h = h0 + j * kRopeWarps;  // the same for every lane
+            if (h >= heads) break;
+            if (h >= a.Hq + a.Hkv) {  // v: copy into the cache
+                const int hv = h - a.Hq - a.Hkv;
+                __nv_bfloat16* dst = a.v_cache + ((page * a.Hkv + hv) * a.page_size + off) * kD;
+                *reinterpret_cast<uint32_t*>(dst + i0) = lo[j];
+                *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = hi[j];
+                continue;
             }
-            // every lane runs the shuffles; only q/k heads with a weight use them
-            float ss = 0.f;
+            float x[4] = {__uint_as_float(lo[j] << 16), __uint_as_float(lo[j] & 0xffff0000u),
+                          __uint_as_float(hi[j] << 16), __uint_as_float(hi[j] & 0xffff0000u)};
+            const bool is_q = h < a.Hq;
+            if (is_q ? a.q_norm_w != nullptr : a.k_norm_w != nullptr) {
+                float ss = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);
+                for (int e = 0; e < 4; ++e) ss = __fmaf_rn(x[e], x[e], ss);
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const bool norm = !is_v && (is_q ? a.q_norm_w != nullptr : a.k_norm_w != nullptr);
-            if (norm) {
+                for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 const float r = rsqrtf(__fdiv_rn(ss, static_cast<float>(kD)) + a.eps);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
+                for (int e = 0; e < 4; ++e)
                     x[e] = __bfloat162float(
                         __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[e], r), is_q ? qw[e] : kw[e])));
             }
-            float y[8];
+            float y[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float other = __shfl_xor_sync(0xffffffffu, x[e], 8);  // rotation partner
-                y[e] = first ? __fsub_rn(__fmul_rn(x[e], c[e]), __fmul_rn(other, sn[e]))
-                             : __fadd_rn(__fmul_rn(x[e], c[e]), __fmul_rn(other, sn[e]));
+            for (int e = 0; e < 2; ++e) {
+                y[e] = __fsub_rn(__fmul_rn(x[e], c[e]), __fmul_rn(x[2 + e], sn[e]));
+                y[2 + e] = __fadd_rn(__fmul_rn(x[2 + e], c[e]), __fmul_rn(x[e], sn[e]));
             }
-            if (!valid) continue;
             __nv_bfloat16* dst;
-            uint4 o;
-            if (is_v) {
-                dst = a.v_cache + ((page * a.Hkv + (h - a.Hq - a.Hkv)) * a.page_size + off) * kD;
-                o = xv[j];
+            if (is_q) {
+                dst = a.q_out + (static_cast<int64_t>(t) * a.Hq + h) * kD;
             } else {
-                dst = is_q ? a.q_out + (static_cast<int64_t>(t) * a.Hq + h) * kD
-                           : a.k_cache + ((page * a.Hkv + (h - a.Hq)) * a.page_size + off) * kD;
-                o = make_uint4(bi::pack_bf16x2(y[0], y[1]), bi::pack_bf16x2(y[2], y[3]),
-                               bi::pack_bf16x2(y[4], y[5]), bi::pack_bf16x2(y[6], y[7]));
+                dst = a.k_cache + ((page * a.Hkv + (h - a.Hq)) * a.page_size + off) * kD;
             }
-            *reinterpret_cast<uint4*>(dst + d0) = o;
+            *reinterpret_cast<uint32_t*>(dst + i0) = bi::pack_bf16x2(y[0], y[1]);
+            *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = bi::pack_bf16x2(y[2], y[3]);
         }
     }
 }
