@@ -18,7 +18,6 @@ bi_prefill_attention; both give a token the same bits.
 """
 from __future__ import annotations
 
-import math
 from collections import deque
 from dataclasses import dataclass, field
 

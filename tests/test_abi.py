@@ -2,7 +2,6 @@
 every entry point include/bi.h declares, and rejects invalid arguments before
 touching the device.  No call here launches a kernel (the pointers passed are
 never dereferenced: validation fails first)."""
-import ctypes
 import os
 import re
 

@@ -10,7 +10,6 @@ allows), the rotation carries that into both outputs of the pair, and the
 output is rounded once more -- and since a rotation can cancel, the bound is
 on the pair's length rather than on each element.
 """
-import math
 
 import numpy as np
 import pytest
