@@ -69,7 +69,7 @@ def parse_args():
     ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "gemm_layers", "attention",
                                        "rmsnorm", "decoder", "prefill", "add_rmsnorm",
                                        "logprobs", "qk_norm_rope_append", "silu_mul",
-                                       "gemm_swiglu"],
+                                       "gemm_swiglu", "decode_latency"],
                     help="time one kernel of the path alone (for profiling); prints its own line")
     ap.add_argument("--requests", type=int, default=1000, help="--case decoder: requests")
     ap.add_argument("--layers", type=int, default=36, help="--case decoder: decoder layers")
@@ -978,10 +978,45 @@ def run_decoder(args):
     print(json.dumps(result), flush=True)
 
 
+def run_decode_latency(args):
+    """Small-batch decode on the random-init Qwen3-8B-shaped decoder: B
+    requests of 128 prompt tokens each generate 64 tokens; ms per decode step
+    with eager launches and with CUDA-graph steps (bit-identical logits; the
+    graphs remove per-launch host work).  Wall clock of the whole generate
+    call divided by its steps, after a warm-up run that captures the graphs."""
+    import __graft_entry__
+    from invariant_bi_rmsnorm_gb300 import qwen3
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    cfg = qwen3.Qwen3Config(layers=args.layers)
+    w = qwen3.Qwen3Weights(cfg, seed=1000)
+    out = {"case": "decode_latency", "layers": args.layers, "prompt_len": 128,
+           "new_tokens": 64, "unit": "ms per step"}
+    for B in (1, 8, 64, 256):
+        row = {}
+        for graphs in (False, True):
+            eng = qwen3.Engine(w, num_pages=B * 16 + 64, max_tokens_per_step=8192,
+                               cuda_graphs=graphs)
+            eng.generate(qwen3.random_requests(B, cfg.vocab, 128, 128, 4, seed=6))
+            eng.reset()
+            reqs = qwen3.random_requests(B, cfg.vocab, 128, 128, 64, seed=5)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            eng.generate(reqs)
+            torch.cuda.synchronize()
+            row["graphs" if graphs else "eager"] = round((time.perf_counter() - t0) / eng.steps * 1e3, 3)
+            del eng
+            torch.cuda.empty_cache()
+        out[str(B)] = row
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse_args()
     if args.case == "decoder":
         run_decoder(args)
+    elif args.case == "decode_latency":
+        run_decode_latency(args)
     elif args.case:
         run_case(args)
     elif args.impl == "reference":

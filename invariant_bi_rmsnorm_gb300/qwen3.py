@@ -24,8 +24,9 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import (add_rmsnorm, decode_attention, gemm, gemm_swiglu, interleave_gate_up, logprobs,
-               prefill_attention, qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
+from . import (add_rmsnorm, decode_attention, decode_attention_workspace_size, gemm,
+               gemm_swiglu, interleave_gate_up, logprobs, prefill_attention,
+               qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
 from . import inputs
 from ._lib import PAGE_SIZE
 
@@ -101,11 +102,20 @@ class Engine:
     """Paged KV cache + continuous-batching greedy decode over Qwen3Weights
     (optionally truncated to the first n_layers layers)."""
 
+    GRAPH_BUCKETS = (1, 2, 4, 8, 16, 32, 64, 128, 256)
+
     def __init__(self, weights: Qwen3Weights, num_pages: int, max_tokens_per_step: int = 8192,
-                 n_layers: int | None = None, device="cuda", ops: str = "bi"):
+                 n_layers: int | None = None, device="cuda", ops: str = "bi",
+                 cuda_graphs: bool = False):
         """ops="bi": every GEMM and RMSNorm through this library (batch-invariant).
         ops="torch": GEMMs through torch.matmul (cuBLAS) and RMSNorms through
-        torch.nn.functional.rms_norm instead -- the non-invariant comparison."""
+        torch.nn.functional.rms_norm instead -- the non-invariant comparison.
+        cuda_graphs: run decode-only steps of up to 256 sequences as a CUDA
+        graph captured once per batch bucket (1, 2, 4, ... 256 rows), padded
+        with rows that read and write one reserved page.  The kernels are the
+        same, and no row's arithmetic depends on the others, so the logits are
+        the same bits as without graphs; what goes away is the per-launch host
+        work of about 300 launches a step."""
         if ops not in ("bi", "torch"):
             raise ValueError("ops must be 'bi' or 'torch'")
         self.ops = ops
@@ -119,7 +129,14 @@ class Engine:
         self.k_cache = [torch.empty(num_pages, Hkv, PAGE_SIZE, D, dtype=torch.bfloat16,
                                     device=self.device) for _ in range(self.n_layers)]
         self.v_cache = [torch.empty_like(k) for k in self.k_cache]
-        self.free_pages = deque(range(num_pages))
+        self.cuda_graphs = cuda_graphs
+        if cuda_graphs and num_pages < 2:
+            raise ValueError("cuda_graphs needs a spare page for padding rows")
+        # with graphs, the last page belongs to the padding rows
+        self.pad_page = num_pages - 1 if cuda_graphs else None
+        self.free_pages = deque(range(num_pages - 1 if cuda_graphs else num_pages))
+        self._graphs = {}
+        self.graph_steps = 0
         self.rope = rope_table(cfg.max_pos, cfg.rope_theta, D, device=self.device)
         T, H, F = max_tokens_per_step, cfg.hidden, cfg.ffn
         e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=self.device)  # noqa: E731
@@ -220,6 +237,19 @@ class Engine:
                            int(max(nqs)), int(max(lens)))
 
         b = {k: v[:T] for k, v in self.buf.items()}
+        self._layers(b, T, tok_d, pos_d, slot_d, meta)
+        samp = [int(offs[k + 1] - 1) for k, want in enumerate(want_logits) if want]
+        if not samp:
+            return None
+        nrows = torch.index_select(b["n"], 0, up(samp, np.int64))
+        self.steps += 1
+        return gemm(nrows, self.w.lm_head, out=torch.empty(len(samp), cfg.vocab,
+                                                           dtype=torch.bfloat16, device=dev))
+
+    def _layers(self, b, T, tok_d, pos_d, slot_d, meta):
+        """Embedding, every decoder layer and the final norm for the step's T
+        token rows (into b["n"])."""
+        cfg = self.cfg
         res = b["res"]
         gemm, rmsnorm, add_rmsnorm = self._ops()
         torch.index_select(self.w.embed, 0, tok_d, out=res)
@@ -244,13 +274,83 @@ class Engine:
                 silu_mul(b["gu"], out=b["h"])
             gemm(b["h"], L["down"], out=b["d"])
         add_rmsnorm(b["d"], res, self.w.final_norm, cfg.eps, out=b["n"])
-        samp = [int(offs[k + 1] - 1) for k, want in enumerate(want_logits) if want]
-        if not samp:
-            return None
-        nrows = torch.index_select(b["n"], 0, up(samp, np.int64))
+
+    # ----------------------------------------------------------- graphs ----
+    def _graph_for(self, Bb: int):
+        """The captured decode step for Bb rows, with its static inputs."""
+        if Bb in self._graphs:
+            return self._graphs[Bb]
+        cfg, dev = self.cfg, self.device
+        W = cfg.max_pos // PAGE_SIZE
+        i32 = dict(dtype=torch.int32, device=dev)
+        st = {"tok": torch.zeros(Bb, dtype=torch.int64, device=dev),
+              "pos": torch.zeros(Bb, **i32),
+              "slot": torch.full((Bb,), self.pad_page * PAGE_SIZE, **i32),
+              "lens": torch.ones(Bb, **i32),
+              "bt": torch.full((Bb, W), self.pad_page, **i32),
+              "logits": torch.empty(Bb, cfg.vocab, dtype=torch.bfloat16, device=dev),
+              "ws": torch.empty(decode_attention_workspace_size(Bb, cfg.heads, cfg.head_dim,
+                                                                cfg.max_pos),
+                                dtype=torch.uint8, device=dev)}
+        meta = {"dec": (slice(0, Bb), st["bt"], st["lens"], cfg.max_pos, W), "ws": st["ws"]}
+        b = {k: v[:Bb] for k, v in self.buf.items()}
+        gemm_, _, _ = self._ops()
+
+        def body():
+            self._layers(b, Bb, st["tok"], st["pos"], st["slot"], meta)
+            gemm_(b["n"], self.w.lm_head, out=st["logits"])
+
+        # one eager run first (library set-up happens outside the capture)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            body()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body()
+        self._graphs[Bb] = (g, st)
+        return self._graphs[Bb]
+
+    def _graph_step(self, items, pending):
+        """A decode-only step through the captured graph of its bucket.
+        Returns logits [len(items), vocab] (valid until the next replay)."""
+        B = len(items)
+        Bb = next(x for x in self.GRAPH_BUCKETS if x >= B)
+        g, st = self._graph_for(Bb)
+        W = st["bt"].shape[1]
+        tok = np.zeros(Bb, dtype=np.int64)
+        pos = np.zeros(Bb, dtype=np.int32)
+        slot = np.full(Bb, self.pad_page * PAGE_SIZE, dtype=np.int32)
+        lens = np.ones(Bb, dtype=np.int32)
+        bt = np.full((Bb, W), self.pad_page, dtype=np.int32)
+        fill_rows, fill_src = [], []
+        src_of = pending[1] if pending is not None else {}
+        for r, (seq, _) in enumerate(items):
+            t0 = seq.n_cached
+            self._ensure_pages(seq, t0 + 1)
+            j = src_of.get(id(seq))
+            if j is not None:
+                fill_rows.append(r)
+                fill_src.append(j)
+            else:
+                tok[r] = seq.tokens[t0]
+            pos[r] = t0
+            slot[r] = seq.pages[t0 // PAGE_SIZE] * PAGE_SIZE + t0 % PAGE_SIZE
+            lens[r] = t0 + 1
+            bt[r, :len(seq.pages)] = seq.pages
+        for name, arr in (("tok", tok), ("pos", pos), ("slot", slot), ("lens", lens), ("bt", bt)):
+            st[name].copy_(torch.from_numpy(arr).pin_memory(), non_blocking=True)
+        if fill_rows:
+            idx = torch.from_numpy(np.asarray(fill_rows, dtype=np.int64)).pin_memory().to(
+                self.device, non_blocking=True)
+            src = torch.from_numpy(np.asarray(fill_src, dtype=np.int64)).pin_memory().to(
+                self.device, non_blocking=True)
+            st["tok"][idx] = pending[0][src]
+        g.replay()
         self.steps += 1
-        return gemm(nrows, self.w.lm_head, out=torch.empty(len(samp), cfg.vocab,
-                                                           dtype=torch.bfloat16, device=dev))
+        self.graph_steps += 1
+        return st["logits"][:B]
 
     def _ops(self):
         if self.ops == "bi":
@@ -291,7 +391,8 @@ class Engine:
                 q, out = torch.index_select(b["q"], 0, rows), None
             if kind == "dec":
                 _, bt, lens, mx, _ = meta[kind]
-                out = decode_attention(q, kc, vc, bt, lens, max_seq_len=mx, out=out)
+                out = decode_attention(q, kc, vc, bt, lens, max_seq_len=mx, out=out,
+                                       workspace=meta.get("ws"))
             else:
                 _, bt, lens, indptr, mq, mx = meta[kind]
                 out = prefill_attention(q, kc, vc, bt, lens, indptr, max_q_len=mq,
@@ -332,7 +433,11 @@ class Engine:
                 else:
                     break
             want = [s.n_cached + n == len(s.tokens) for s, n in items]
-            logits = self.forward(items, want, pending=prev[:2] if prev else None)
+            decode_only = all(n == 1 and s.n_cached >= len(s.prompt) for s, n in items)
+            if self.cuda_graphs and decode_only and 0 < len(items) <= self.GRAPH_BUCKETS[-1]:
+                logits = self._graph_step(items, prev[:2] if prev else None)
+            else:
+                logits = self.forward(items, want, pending=prev[:2] if prev else None)
             if prev is not None:
                 self._resolve(prev)
             prev = None
@@ -389,8 +494,9 @@ class Engine:
             s.generated[-1] = int(vals[j])
 
     def reset(self):
-        self.free_pages = deque(range(self.num_pages))
+        self.free_pages = deque(range(self.num_pages - 1 if self.cuda_graphs else self.num_pages))
         self.steps = 0
+        self.graph_steps = 0
 
 
 def random_requests(n: int, vocab: int, min_len: int, max_len: int, max_new: int,
