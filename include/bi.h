@@ -115,8 +115,8 @@ bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y, 
  *
  * Operation: "2. Batch-Invariant Matrix Multiplication" of the same page: a
  * data-parallel tiled matmul with ONE kernel configuration for every shape --
- * a fixed 256x224 output tile computed by a pair of CTAs (tcgen05.mma
- * cta_group::2, M=256, N=224, K=16), K walked in ascending 64-wide blocks,
+ * a fixed 256x256 output tile computed by a pair of CTAs (tcgen05.mma
+ * cta_group::2, M=256, N=256, K=16), K walked in ascending 64-wide blocks,
  * each block as four ascending 16-deep MMAs accumulating in TMEM.  No split-K
  * or stream-K for any M, and the same MMA instruction shape always.
  *

@@ -6,14 +6,14 @@
 // data-parallel matmul gives each output tile to one core and reduces its
 // whole K range there; splitting K when M*N is small, or switching tensor-core
 // instruction or tile shape with the batch size, changes the reduction order.
-// So this kernel has exactly one tile shape (256 x 224, computed by a pair of
+// So this kernel has exactly one tile shape (256 x 256, computed by a pair of
 // CTAs on two SMs), one MMA instruction shape (tcgen05.mma.cta_group::2
-// kind::f16, M=256, N=224, K=16) and one K order (64-wide blocks ascending,
+// kind::f16, M=256, N=256, K=16) and one K order (64-wide blocks ascending,
 // each as 4 ascending 16-deep MMAs into one fp32 TMEM accumulator), whatever
 // M, N and K are.  No split-K, no stream-K.
 //
 // Structure (persistent, one CTA pair per two SMs, warp-specialised):
-//   warp 0      TMA producer in each CTA: its 128 rows of x and its 112 rows
+//   warp 0      TMA producer in each CTA: its 128 rows of x and its 128 rows
 //               of W (64-wide K slabs, 128-byte swizzle) into a 7-stage ring;
 //               both CTAs' copies complete on the leader CTA's barrier;
 //   warp 1      allocates 512 TMEM columns in both CTAs (two accumulators);
@@ -66,7 +66,7 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
 namespace pair {
 constexpr int BMP = 256;  // pair tile rows
 constexpr int BMC = 128;  // rows per CTA
-constexpr int BN = 224;
+constexpr int BN = 256;
 constexpr int BNC = BN / 2;  // W rows per CTA
 constexpr int BK = 64;
 constexpr int kStages = 7;
@@ -302,7 +302,7 @@ bi_status launch_gemm(const void* x, const void* W, void* y, int32_t M, int32_t 
     if (!x || !W || !y) return BI_ERR_INVALID_ARG;
     if (!bi::aligned16(x) || !bi::aligned16(W) || !bi::aligned16(y)) return BI_ERR_MISALIGNED;
 
-    // TMA boxes: each CTA loads 128 rows of x and 112 rows of W per 64-wide K slab
+    // TMA boxes: each CTA loads 128 rows of x and 128 rows of W per 64-wide K slab
     CUtensorMap tx, tw;
     if (bi::encode_tensor_map_2d(&tx, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                                  static_cast<uint64_t>(ld_x) * 2, pair::BK, pair::BMC) != CUDA_SUCCESS ||
