@@ -449,12 +449,11 @@ class Engine:
                 forced = [(j, s.forced[len(s.generated)]) for j, s in enumerate(sampled)
                           if s.forced is not None]
                 if forced:
-                    fj = torch.tensor([j for j, _ in forced], dtype=torch.int64, device=self.device)
-                    fv = torch.tensor([v for _, v in forced], dtype=torch.int64, device=self.device)
-                    picks[fj] = fv
+                    fj = self._up([j for j, _ in forced])
+                    picks[fj] = self._up([v for _, v in forced])
                 rec = [(j, s.sid) for j, s in enumerate(sampled) if s.sid in record]
                 if rec:
-                    rj = torch.tensor([j for j, _ in rec], dtype=torch.int64, device=self.device)
+                    rj = self._up([j for j, _ in rec])
                     lg = torch.index_select(logits, 0, rj)
                     lps, _ = logprobs(lg, picks[rj].to(torch.int32))
                     for i, (_, sid) in enumerate(rec):
@@ -481,6 +480,13 @@ class Engine:
             logs[sid] = list(lg.unbind(0)) if rows else []
             self.logprobs[sid] = list(lp.unbind(0)) if rows else []
         return logs
+
+    def _up(self, values):
+        """int64 host list -> device tensor through pinned memory, without
+        waiting for the device (a plain torch.tensor(..., device=...) copy from
+        pageable memory would stall the host until the stream drains)."""
+        return torch.from_numpy(np.asarray(values, dtype=np.int64)).pin_memory().to(
+            self.device, non_blocking=True)
 
     @staticmethod
     def _resolve(prev):
