@@ -96,6 +96,23 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_page_map(CUtensorMap* map, const void* base, uint64_t rows) {
+    CUtensorMap probe;
+    const CUresult r = encode_tensor_map_2d(&probe, base, 128, rows, 256, 64, 16);  // resolves the entry point
+    if (r != CUDA_SUCCESS) return r;
+    // dims: 64 dims of a half-row (inner), token rows (256-byte stride), the
+    // two halves of a row (128-byte stride); one box = a 16-row page block,
+    // stored half 0 then half 1, as two 16 x 64 boxes would be
+    cuuint64_t dims[3] = {64, rows, 2};
+    cuuint64_t strides[2] = {256, 128};
+    cuuint32_t box[3] = {64, 16, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace bi
 
 extern "C" {

@@ -16,9 +16,10 @@
 // Each output element of an mma depends only on its own column, so a column's
 // result does not depend on what shares the tile with it.
 //
-// Shared-memory layout of one page block (K or V), as written by two 16 x 64
-// TMA boxes with the 128-byte swizzle: dims [64*(ch/8), +64) at offset
-// (ch/8)*2048, 128-byte rows, the 16-byte unit index XORed with (row % 8).
+// Shared-memory layout of one page block (K or V), as written by one TMA box
+// of 64 dims x 16 rows x 2 halves with the 128-byte swizzle: dims
+// [64*(ch/8), +64) at offset (ch/8)*2048, 128-byte rows, the 16-byte unit
+// index XORed with (row % 8).
 #pragma once
 #include <cuda_bf16.h>
 

@@ -43,6 +43,11 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner
                               uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner,
                               uint32_t box_outer);
 
+// The K or V cache [num_pages * Hkv * 16 rows][128] as a 3-D map whose box is
+// one 16-row page block in the two-half, 128-byte-swizzled layout of two
+// 16 x 64 boxes (one copy instead of two).
+CUresult encode_page_map(CUtensorMap* map, const void* base, uint64_t rows);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace bi

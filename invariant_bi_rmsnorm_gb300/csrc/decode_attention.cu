@@ -13,8 +13,9 @@
 // to 16 pages of 16 tokens.  Warp w takes chunks c0 + w, c0 + w + 4, ... of
 // the group and, for the Hq/Hkv query heads sharing kv-head g, runs one online
 // softmax over each chunk's pages 0, 1, 2, ... in order (attn_common.cuh
-// gives the per-page arithmetic).  Pages arrive by TMA (2-D tiled loads,
-// 128-byte swizzle) into a 2-stage ring per warp.  A chunk's final state is its
+// gives the per-page arithmetic).  Pages arrive by TMA (one 3-D tiled load
+// per page block of K and of V, 128-byte swizzle) into a 2-stage ring per
+// warp.  A chunk's final state is its
 // partial (m, l, O).  If the CTA's group holds every chunk of the sequence,
 // the partials are folded in ascending chunk order inside the CTA (warp by
 // warp after each round of four chunks) and bf16(O / l) is written; otherwise
@@ -166,10 +167,8 @@ __global__ void __launch_bounds__(kThreads)
             uint8_t* vd = kd + kMatBytes;
             const int row = rows_s[(lc - c0) * ppc + lp];
             bi::mbar_arrive_expect_tx(&bars[st], kStageBytes);
-            bi::tma_load_2d(kd, &tmap_k, &bars[st], 0, row);
-            bi::tma_load_2d(kd + kHalfBytes, &tmap_k, &bars[st], 64, row);
-            bi::tma_load_2d(vd, &tmap_v, &bars[st], 0, row);
-            bi::tma_load_2d(vd + kHalfBytes, &tmap_v, &bars[st], 64, row);
+            bi::tma_load_3d(kd, &tmap_k, &bars[st], 0, row, 0);
+            bi::tma_load_3d(vd, &tmap_v, &bars[st], 0, row, 0);
         }
         ++lj;
         if (++lp >= pages_in(lc)) {
@@ -419,8 +418,8 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
 
     CUtensorMap tk, tv;
     const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv * kPage;
-    if (bi::encode_tensor_map_2d(&tk, k_cache, kD, rows, kD * 2, 64, kPage) != CUDA_SUCCESS ||
-        bi::encode_tensor_map_2d(&tv, v_cache, kD, rows, kD * 2, 64, kPage) != CUDA_SUCCESS)
+    if (bi::encode_page_map(&tk, k_cache, rows) != CUDA_SUCCESS ||
+        bi::encode_page_map(&tv, v_cache, rows) != CUDA_SUCCESS)
         return BI_ERR_CUDA;
 
     int dev = 0;

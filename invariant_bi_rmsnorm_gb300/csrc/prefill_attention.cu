@@ -138,10 +138,8 @@ __global__ void __launch_bounds__(kThreads, BI_PREFILL_MIN_BLOCKS)
                 uint8_t* vd = kd + kMatBytes;
                 const int row = (bt[k] * a.Hkv + g) * kPage;
                 bi::mbar_arrive_expect_tx(&full[st], kStageBytes);
-                bi::tma_load_2d(kd, &tmap_k, &full[st], 0, row);
-                bi::tma_load_2d(kd + kHalfBytes, &tmap_k, &full[st], 64, row);
-                bi::tma_load_2d(vd, &tmap_v, &full[st], 0, row);
-                bi::tma_load_2d(vd + kHalfBytes, &tmap_v, &full[st], 64, row);
+                bi::tma_load_3d(kd, &tmap_k, &full[st], 0, row, 0);
+                bi::tma_load_3d(vd, &tmap_v, &full[st], 0, row, 0);
             }
         }
         return;
@@ -280,8 +278,8 @@ extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, co
 
     CUtensorMap tk, tv;
     const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv * kPage;
-    if (bi::encode_tensor_map_2d(&tk, k_cache, kD, rows, kD * 2, 64, kPage) != CUDA_SUCCESS ||
-        bi::encode_tensor_map_2d(&tv, v_cache, kD, rows, kD * 2, 64, kPage) != CUDA_SUCCESS)
+    if (bi::encode_page_map(&tk, k_cache, rows) != CUDA_SUCCESS ||
+        bi::encode_page_map(&tv, v_cache, rows) != CUDA_SUCCESS)
         return BI_ERR_CUDA;
 
     int dev = 0;
