@@ -7,9 +7,14 @@ computation runs in the library's CUDA kernels.  There is no CPU fallback:
 tensors must live on a CUDA device, and a missing library raises.
 
     rmsnorm(x, w, eps)                    y = x * rsqrt(mean(x^2) + eps) * w, per row
+    add_rmsnorm(x, residual, w, eps)      residual += x, then rmsnorm(residual)
     gemm(x, W)                            y = x @ W.T  (W in nn.Linear [N, K] layout)
+    gemm_swiglu(x, interleave_gate_up(W)) silu(x @ W_gate.T) * (x @ W_up.T), fused
     decode_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_len)
                                           paged decode attention, 256-token splits
+    prefill_attention(...)                causal attention for many rows per sequence,
+                                          bit-identical per row to decode_attention
+    qk_norm_rope_append(...), silu_mul(gate_up), logprobs(logits, targets)
 
 Every output row's bits depend only on that row's own inputs (batch
 invariance); see include/bi.h for the exact contract of each call.
@@ -23,7 +28,8 @@ import torch
 from . import _lib
 from ._lib import DECODE_CHUNK, PAGE_SIZE
 
-__all__ = ["BiError", "rmsnorm", "gemm", "decode_attention", "decode_attention_fixed_splits",
+__all__ = ["BiError", "rmsnorm", "gemm", "gemm_swiglu", "interleave_gate_up",
+           "decode_attention", "decode_attention_fixed_splits",
            "prefill_attention", "add_rmsnorm", "qk_norm_rope_append", "silu_mul",
            "rope_table", "logprobs",
            "decode_attention_workspace_size", "selftest_wait_timeout",
