@@ -649,9 +649,28 @@ def run_e2e(wl, args, dev, barrier, dist, world):
     ms = reduce_max_over_ranks([e0.elapsed_time(e1)], dist, device=dev)[0]
     # the pipelined outputs equal the device-resident run's
     ok = bool(torch.equal(host_out["down"], wl.gy["down"].cpu()))
+    # this box's copy-engine rates, for the floor the step's copies impose
+    probe_h = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
+    probe_d = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def copy_ms(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(3):
+            fn()
+        c1.record()
+        torch.cuda.synchronize(dev)
+        return c0.elapsed_time(c1) / 3
+    h2d_gbs = probe_h.numel() / copy_ms(lambda: probe_d.copy_(probe_h, non_blocking=True)) / 1e6
+    d2h_gbs = probe_h.numel() / copy_ms(lambda: probe_h.copy_(probe_d, non_blocking=True)) / 1e6
+    del probe_h, probe_d
     return {"value": round(weak_scaling_rate(wl.gemm_flops, world, args.steps, ms) / 1e12, 2),
             "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / args.steps, 4), "outputs_match_device_run": ok,
+            "copy_engines_gbs": {"h2d": round(h2d_gbs, 1), "d2h": round(d2h_gbs, 1)},
+            "copy_only_ms_per_step": round(h2d / h2d_gbs / 1e6 + d2h / d2h_gbs / 1e6, 4),
             "what": ("GEMM FLOPs of one step / wall time per step through the Python API with "
                      "every step's inputs copied in from pinned memory and all outputs copied "
                      "out, copies of neighbouring steps overlapping the step's kernels")}
