@@ -26,7 +26,9 @@ Sources: the three reduction ops follow "Defeating Nondeterminism in LLM
 Inference: The Core Role of Batch Invariance" (sections 1-3); the layer
 structure is the Qwen3-8B shape the workload names (pre-norm, GQA 32/8,
 head_dim 128, SwiGLU, RoPE theta 1e6, per-head q/k RMSNorm).
-Pins: tests/test_oracle.py (rope, silu, causal attention closed forms).
+Pins: tests/test_oracle.py (rope, silu, causal attention closed forms; for the
+composition: a layer whose output projections are zero is the identity, the
+zero-layer closed form for a constant embedding row, causality).
 """
 from __future__ import annotations
 

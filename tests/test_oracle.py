@@ -431,3 +431,59 @@ def test_logprobs_against_scipy_and_normalisation():
     np.testing.assert_allclose(lse, logsumexp(xs, axis=1), rtol=1e-13)
     lps = np.stack([oracle.logprobs(x, np.full(3, j))[0] for j in range(0, 2048, 1)], axis=1)
     np.testing.assert_allclose(np.exp(lps).sum(axis=1), 1.0, rtol=1e-12)
+
+
+# ------------------------------------------------- decoder composition -------
+def _tiny_decoder(seed, H=64, F=32, V=40, Hq=2, Hkv=1, zero_blocks=False):
+    """Random bf16 weights of a 1-layer decoder with tiny widths (head dim 128)."""
+    g = torch.Generator().manual_seed(seed)
+
+    def w(*shape, std=0.05, zero=False):
+        t = torch.zeros(shape) if zero else torch.randn(*shape, generator=g) * std
+        return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    ones = lambda n: torch.ones(n, dtype=torch.bfloat16).view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    return {"embed": w(V, H, std=1.0), "lm_head": w(V, H), "final_norm": ones(H),
+            "0.in_norm": ones(H), "0.qkv": w((Hq + 2 * Hkv) * 128, H), "0.q_norm": ones(128),
+            "0.k_norm": ones(128), "0.o": w(H, Hq * 128, zero=zero_blocks),
+            "0.post_norm": ones(H), "0.gate_up": w(2 * F, H),
+            "0.down": w(H, F, zero=zero_blocks)}
+
+
+def test_decoder_layer_with_zero_output_projections_is_the_identity():
+    """With the attention output and MLP down projections zero, a layer adds
+    nothing to the residual stream, so one layer gives exactly the logits of
+    zero layers: catches a wrong residual wiring or a stray rounding."""
+    from oracle import decoder as odec
+    wts = _tiny_decoder(31, zero_blocks=True)
+    toks = np.array([3, 17, 5, 39, 0])
+    one = odec.forward_logits(wts, toks, 1, Hq=2, Hkv=1)
+    zero = odec.forward_logits(wts, toks, 0, Hq=2, Hkv=1)
+    assert np.array_equal(one, zero)
+    # and the layer is not trivial once its projections are non-zero
+    assert not np.array_equal(odec.forward_logits(_tiny_decoder(31), toks, 1, Hq=2, Hkv=1), zero)
+
+
+def test_decoder_zero_layers_closed_form_for_a_constant_embedding():
+    """Zero layers, an embedding row of one constant c and a final norm of
+    ones: the normed row is bf16(c / sqrt(c^2 + eps)) in every element, so the
+    logits are that value times each lm_head row's sum."""
+    from oracle import decoder as odec
+    wts = _tiny_decoder(32)
+    H, c = 64, 0.75
+    row = torch.full((H,), c, dtype=torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    wts["embed"][7] = row
+    got = odec.forward_logits(wts, np.array([7]), 0, Hq=2, Hkv=1)[0]
+    normed = float(torch.tensor(c / math.sqrt(c * c + 1e-6)).to(torch.bfloat16).double())
+    lm = torch.from_numpy(wts["lm_head"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    np.testing.assert_allclose(got, normed * lm.sum(axis=1), rtol=1e-12, atol=1e-12)
+
+
+def test_decoder_is_causal():
+    """A position's logits do not depend on the tokens after it."""
+    from oracle import decoder as odec
+    wts = _tiny_decoder(33)
+    a = odec.forward_logits(wts, np.array([1, 2, 3, 4, 5, 6]), 1, Hq=2, Hkv=1)
+    b = odec.forward_logits(wts, np.array([1, 2, 3, 4, 9, 11]), 1, Hq=2, Hkv=1)
+    assert np.array_equal(a[:4], b[:4])
+    assert not np.array_equal(a[4:], b[4:])
