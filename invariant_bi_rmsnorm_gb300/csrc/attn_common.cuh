@@ -69,27 +69,43 @@ __device__ __forceinline__ void load_q_frags(const __nv_bfloat16* col_q, int lan
     }
 }
 
-// One page.  valid0 / valid1: how many of the page's 16 tokens columns
-// 2(l%4) and 2(l%4)+1 may see (0 .. 16).  A column that sees none of them
-// keeps its state unchanged.
-__device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint32_t vs_base,
+// P^T fragments of one page for one 8-column group: the bf16 high parts and
+// the bf16 remainders (mma B operands, tokens on K, columns on N).
+struct PFrags {
+    uint32_t hi0, hi1, lo0, lo1;
+};
+
+// The page's raw scores S^T = K_page . Q^T for this lane's 4 entries: sc[0],
+// sc[1] are token l/4 for columns 2(l%4) and 2(l%4)+1, sc[2], sc[3] token
+// l/4 + 8.  Eight MMAs over the dims in ascending 16-blocks into one
+// accumulator.
+__device__ __forceinline__ void page_scores(float (&sc)[4], uint32_t ks_base,
                                             const uint32_t (&qb0)[8], const uint32_t (&qb1)[8],
-                                            int valid0, int valid1, float scale_log2, int lane) {
+                                            int lane) {
     const int lm_j = lane >> 3;  // which 8x8 matrix this lane addresses
     const int lm_r = lane & 7;   // row within it
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         uint32_t a0, a1, a2, a3;
         bi::ldmatrix_x4(ks_base + swz(lm_r + 8 * (lm_j & 1), 2 * ks + (lm_j >> 1)), a0, a1, a2, a3);
         bi::mma_bf16_16816(sc, a0, a1, a2, a3, qb0[ks], qb1[ks]);
     }
-    // sc[0], sc[1]: token l/4, columns 2(l%4)+{0,1}; sc[2], sc[3]: token l/4 + 8
+}
+
+// Online-softmax update of one column group from its raw scores: masking,
+// running max, the rescale of l and O, p = 2^(x - m), l += sum p, and p split
+// into bf16 high part + bf16 remainder, transposed into mma B fragments.
+// Every operation is an explicit rounding intrinsic, so the compiler cannot
+// fuse a different pair of them in one caller than in another.
+__device__ __forceinline__ void softmax_step(ColState& st, const float (&sc)[4], int valid0,
+                                             int valid1, float scale_log2, int lane, PFrags& pf) {
     const int tokA = lane >> 2, tokB = tokA + 8;
-    const float x0 = tokA < valid0 ? sc[0] * scale_log2 : -INFINITY;
-    const float x1 = tokA < valid1 ? sc[1] * scale_log2 : -INFINITY;
-    const float x2 = tokB < valid0 ? sc[2] * scale_log2 : -INFINITY;
-    const float x3 = tokB < valid1 ? sc[3] * scale_log2 : -INFINITY;
+    const float x0 = tokA < valid0 ? __fmul_rn(sc[0], scale_log2) : -INFINITY;
+    const float x1 = tokA < valid1 ? __fmul_rn(sc[1], scale_log2) : -INFINITY;
+    const float x2 = tokB < valid0 ? __fmul_rn(sc[2], scale_log2) : -INFINITY;
+    const float x3 = tokB < valid1 ? __fmul_rn(sc[3], scale_log2) : -INFINITY;
     float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
     for (int off = 4; off <= 16; off <<= 1) {
@@ -98,12 +114,12 @@ __device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint
     }
     const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
     // a column with no visible token so far keeps m = -inf: no rescale, p = 0
-    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(st.m[0] - mn0);
-    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(st.m[1] - mn1);
-    const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mn0);
-    const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mn1);
-    const float p2 = x2 == -INFINITY ? 0.f : exp2f(x2 - mn0);
-    const float p3 = x3 == -INFINITY ? 0.f : exp2f(x3 - mn1);
+    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(__fsub_rn(st.m[0], mn0));
+    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(__fsub_rn(st.m[1], mn1));
+    const float p0 = x0 == -INFINITY ? 0.f : exp2f(__fsub_rn(x0, mn0));
+    const float p1 = x1 == -INFINITY ? 0.f : exp2f(__fsub_rn(x1, mn1));
+    const float p2 = x2 == -INFINITY ? 0.f : exp2f(__fsub_rn(x2, mn0));
+    const float p3 = x3 == -INFINITY ? 0.f : exp2f(__fsub_rn(x3, mn1));
     const uint32_t pA = bi::pack_bf16x2(p0, p1);  // high parts
     const uint32_t pB = bi::pack_bf16x2(p2, p3);
     const uint32_t rA = bi::pack_bf16x2(__fsub_rn(p0, __uint_as_float(pA << 16)),
@@ -114,8 +130,8 @@ __device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint
     float ps1 = __fadd_rn(p1, p3);
 #pragma unroll
     for (int off = 4; off <= 16; off <<= 1) {
-        ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
-        ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+        ps0 = __fadd_rn(ps0, __shfl_xor_sync(0xffffffffu, ps0, off));
+        ps1 = __fadd_rn(ps1, __shfl_xor_sync(0xffffffffu, ps1, off));
     }
     st.l[0] = __fmaf_rn(st.l[0], al0, ps0);
     st.l[1] = __fmaf_rn(st.l[1], al1, ps1);
@@ -123,23 +139,44 @@ __device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint
     st.m[1] = mn1;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-        st.acc[mt][0] *= al0;
-        st.acc[mt][1] *= al1;
-        st.acc[mt][2] *= al0;
-        st.acc[mt][3] *= al1;
+        st.acc[mt][0] = __fmul_rn(st.acc[mt][0], al0);
+        st.acc[mt][1] = __fmul_rn(st.acc[mt][1], al1);
+        st.acc[mt][2] = __fmul_rn(st.acc[mt][2], al0);
+        st.acc[mt][3] = __fmul_rn(st.acc[mt][3], al1);
     }
     // P^T fragments (tokens on K, columns on N) by an in-register transpose
-    const uint32_t pb0 = bi::movmatrix_trans(pA);
-    const uint32_t pb1 = bi::movmatrix_trans(pB);
-    const uint32_t lb0 = bi::movmatrix_trans(rA);
-    const uint32_t lb1 = bi::movmatrix_trans(rB);
+    pf.hi0 = bi::movmatrix_trans(pA);
+    pf.hi1 = bi::movmatrix_trans(pB);
+    pf.lo0 = bi::movmatrix_trans(rA);
+    pf.lo1 = bi::movmatrix_trans(rB);
+}
+
+// O^T += V^T . P_hi^T, then += V^T . P_lo^T, per 16-dim tile in ascending
+// order.
+__device__ __forceinline__ void pv_step(ColState& st, const PFrags& pf, uint32_t vs_base,
+                                        int lane) {
+    const int lm_j = lane >> 3;
+    const int lm_r = lane & 7;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         uint32_t a0, a1, a2, a3;
         bi::ldmatrix_x4_trans(vs_base + swz(lm_r + 8 * (lm_j >> 1), 2 * mt + (lm_j & 1)), a0, a1, a2, a3);
-        bi::mma_bf16_16816(st.acc[mt], a0, a1, a2, a3, pb0, pb1);
-        bi::mma_bf16_16816(st.acc[mt], a0, a1, a2, a3, lb0, lb1);
+        bi::mma_bf16_16816(st.acc[mt], a0, a1, a2, a3, pf.hi0, pf.hi1);
+        bi::mma_bf16_16816(st.acc[mt], a0, a1, a2, a3, pf.lo0, pf.lo1);
     }
+}
+
+// One page for one 8-column group.  valid0 / valid1: how many of the page's
+// 16 tokens columns 2(l%4) and 2(l%4)+1 may see (0 .. 16).  A column that sees
+// none of them keeps its state unchanged.
+__device__ __forceinline__ void attend_page(ColState& st, uint32_t ks_base, uint32_t vs_base,
+                                            const uint32_t (&qb0)[8], const uint32_t (&qb1)[8],
+                                            int valid0, int valid1, float scale_log2, int lane) {
+    float sc[4];
+    page_scores(sc, ks_base, qb0, qb1, lane);
+    PFrags pf;
+    softmax_step(st, sc, valid0, valid1, scale_log2, lane, pf);
+    pv_step(st, pf, vs_base, lane);
 }
 
 // Zero V rows [valid, 16) of a page block in shared memory (one warp).
