@@ -84,3 +84,36 @@ def test_cuda_graph_decode_steps_bit_identical(two_layer):
         assert r0[sid].generated == r1[sid].generated, f"sequence {sid}: tokens differ"
         for step, (a, b) in enumerate(zip(l0[sid], l1[sid])):
             assert np.array_equal(bits(a), bits(b)), f"sequence {sid}: logits differ at step {step}"
+
+
+def test_tiny_requests_and_staggered_finishes(two_layer):
+    """One-token prompts, one-token generations and requests finishing at
+    different steps, with a budget that splits the longest prompt: the same
+    tokens and logits alone as batched, eager and graphed."""
+    cfg, w = two_layer
+    g = torch.Generator().manual_seed(77)
+    spec = [(1, 1), (1, 5), (2, 3), (40, 2), (130, 4)]   # (prompt length, new tokens)
+
+    def make():
+        out = []
+        for i, (L, n) in enumerate(spec):
+            prompt = torch.randint(0, cfg.vocab, (L,), generator=torch.Generator().manual_seed(500 + i)).tolist()
+            out.append(qwen3.Sequence(sid=i, prompt=prompt, max_new=n))
+        return out
+    results = []
+    for graphs in (False, True):
+        eng = qwen3.Engine(w, num_pages=40, max_tokens_per_step=64, cuda_graphs=graphs)
+        reqs = make()
+        logs = eng.generate(reqs, record=set(range(len(spec))))
+        assert all(len(r.generated) == n for r, (_, n) in zip(reqs, spec))
+        results.append((reqs, logs))
+        for i in (0, 4):
+            eng.reset()
+            one = make()[i]
+            alone = eng.generate([one], record={i})
+            assert one.generated == reqs[i].generated
+            assert all(np.array_equal(bits(a), bits(b)) for a, b in zip(alone[i], logs[i]))
+    (r0, l0), (r1, l1) = results
+    for i in range(len(spec)):
+        assert r0[i].generated == r1[i].generated
+        assert all(np.array_equal(bits(a), bits(b)) for a, b in zip(l0[i], l1[i]))
