@@ -213,8 +213,10 @@ __global__ void __launch_bounds__(kThreads)
                 const uint32_t kb = bi::smem_u32(stage_ptr(stg));
                 bi_attn::attend_page(st, kb, kb + kMatBytes, qb0, qb1, valid, valid, a.scale_log2,
                                      lane);
-                // hand the stage back to TMA for this warp's page kSPW ahead
-                bi::fence_proxy_async_smem();
+                // hand the stage back to TMA for this warp's page kSPW ahead; the
+                // zeroed V tail (generic-proxy writes) must be ordered before the
+                // next copy (an async-proxy write) into the same stage
+                if (valid < kPage) bi::fence_proxy_async_smem();
                 __syncwarp();
                 issue_next();
             }
