@@ -545,6 +545,8 @@ def run_ours(args):
         "negative_controls": controls,
         "clocks": clk,
         "gpu_launches": wl.launches_per_step * K,
+        # which kernel sources this line measured (the box has no git metadata)
+        "kernel_sources_sha256_16": {k: kernel_source_sha(v) for k, v in KERNEL_SOURCES.items()},
     }
     if e2e is not None:
         line["e2e"] = e2e
