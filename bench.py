@@ -137,6 +137,9 @@ def traffic_record(kernel: str):
 
 # ----------------------------------------------------------------- clocks ---
 class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons, every 100 ms,
+    read by a thread and stamped with the host clock, so the samples that
+    fall inside a measurement window can be picked out."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -144,8 +147,11 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
         self.device_index = device_index
+        self.lines = []
+        self.thread = None
 
-    def start(self):
+    def start(self, wait_s: float = 3.0):
+        """Start sampling; returns once the first sample has arrived (or after wait_s)."""
         try:
             pci = torch.cuda.get_device_properties(self.device_index)
             sel = ["-i", str(self.device_index)]
@@ -162,26 +168,42 @@ class ClockSampler:
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+        import threading
 
-    def stop(self):
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.perf_counter(), line))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        t0 = time.perf_counter()
+        while not self.lines and time.perf_counter() - t0 < wait_s:
+            time.sleep(0.01)
+
+    def stop(self, window=None):
+        """Summary of the samples stamped inside window = (t0, t1) (host
+        perf_counter seconds), or of all samples."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        time.sleep(0.25)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out = ""
-        sm, smax, reasons = [], [], set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for t, line in self.lines:
+            if window is not None and not (window[0] <= t <= window[1]):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 7:
                 continue
             try:
                 sm.append(float(f[0]))
                 smax.append(float(f[1]))
+                power.append(float(f[2]))
             except ValueError:
                 continue
             for n, v in zip(names, f[3:7]):
@@ -189,6 +211,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "power_w": round(statistics.median(power), 1) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -462,12 +485,26 @@ def run_ours(args):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
+    h0 = time.perf_counter()
     t_start.record(wl.stream)
     for i in range(args.steps):
         wl.step(evs[i])
     t_end.record(wl.stream)
     barrier()
-    clk = clocks.stop()
+    # The timed steps can be shorter than the sampling interval. So the same step keeps
+    # running, untimed, for SOAK_S more seconds. The clocks are taken over the timed steps
+    # and that continuation.
+    while time.perf_counter() - h0 < SOAK_S:
+        for _ in range(20):
+            wl.step()
+        torch.cuda.synchronize(dev)
+    h1 = time.perf_counter()
+    barrier()
+    clk = clocks.stop(window=(h0, h1))
+    clk["window_s"] = round(h1 - h0, 3)
+    clk["window"] = "the timed steps plus an untimed continuation of the same step"
+    if "sw_power_cap" in clk.get("reasons", []):
+        clk["note"] = "software power cap active under the dense GEMMs"
     total_ms = t_start.elapsed_time(t_end)
     rms_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
     gemm_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
@@ -557,6 +594,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+SOAK_S = 0.6  # seconds of the bench step under the clock sampler (timed steps included)
 E2E_BUFFER_SETS = 2  # 3 or 4 sets measured the same: the copy engines are the bound
 
 
