@@ -61,6 +61,19 @@ __device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
     return *reinterpret_cast<const uint32_t*>(p);
 }
 
+__device__ __forceinline__ void load_heads(const __nv_bfloat16* row, int h0, int heads, int i0,
+                                           uint32_t (&lo)[kHeadsPerPass],
+                                           uint32_t (&hi)[kHeadsPerPass]) {
+#pragma unroll
+    for (int j = 0; j < kHeadsPerPass; ++j) {
+        const int h = h0 + j * kRopeWarps;
+        if (h < heads) {
+            lo[j] = ld_b32(row + static_cast<int64_t>(h) * kD + i0);
+            hi[j] = ld_b32(row + static_cast<int64_t>(h) * kD + kHalf + i0);
+        }
+    }
+}
+
 // six CTAs (48 warps) per SM: capping registers at 40 ran 10 % faster than the
 // natural 61 (four CTAs); at 32 the spills cost more than the extra CTAs gave
 __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel(const RopeArgs a) {
@@ -68,13 +81,18 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int heads = a.Hq + 2 * a.Hkv;
+    const int i0 = 2 * lane;
+    const __nv_bfloat16* row = a.qkv + static_cast<int64_t>(t) * a.ld_qkv;
+    // the first pass's q/k/v loads go out before the position is known, so
+    // their latency overlaps that of the position -> RoPE-table chain
+    uint32_t lo[kHeadsPerPass], hi[kHeadsPerPass];
+    load_heads(row, warp, heads, i0, lo, hi);
     const int pos = a.positions[t];
     const int64_t slot = a.slots[t];
     if (pos < 0 || pos >= a.max_pos || slot < 0 || slot >= a.num_slots) {
         if (threadIdx.x == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereDecoderOps);
         return;
     }
-    const int i0 = 2 * lane;
     const float* cs = a.rope + static_cast<int64_t>(pos) * kD;
     const float2 cosv = *reinterpret_cast<const float2*>(cs + i0);
     const float2 sinv = *reinterpret_cast<const float2*>(cs + kHalf + i0);
@@ -86,26 +104,19 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
         qw[e] = a.q_norm_w ? bf(a.q_norm_w[idx[e]]) : 0.f;
         kw[e] = a.k_norm_w ? bf(a.k_norm_w[idx[e]]) : 0.f;
     }
-    const int64_t page = slot / a.page_size, off = slot % a.page_size;
-    const __nv_bfloat16* row = a.qkv + static_cast<int64_t>(t) * a.ld_qkv;
+    // the token's slot in every kv-head's page block (page size fixed at BI_PAGE_SIZE)
+    const int64_t page = slot / BI_PAGE_SIZE, off = slot % BI_PAGE_SIZE;
+    const int64_t kv_slot = (page * a.Hkv * BI_PAGE_SIZE + off) * kD;
 
     for (int h0 = warp; h0 < heads; h0 += kRopeWarps * kHeadsPerPass) {
-        uint32_t lo[kHeadsPerPass], hi[kHeadsPerPass];
-#pragma unroll
-        for (int j = 0; j < kHeadsPerPass; ++j) {
-            const int h = h0 + j * kRopeWarps;
-            if (h < heads) {
-                lo[j] = ld_b32(row + static_cast<int64_t>(h) * kD + i0);
-                hi[j] = ld_b32(row + static_cast<int64_t>(h) * kD + kHalf + i0);
-            }
-        }
+        if (h0 != warp) load_heads(row, h0, heads, i0, lo, hi);
 #pragma unroll
         for (int j = 0; j < kHeadsPerPass; ++j) {
             const int h = h0 + j * kRopeWarps;  // the same for every lane
             if (h >= heads) break;
             if (h >= a.Hq + a.Hkv) {  // v: copy into the cache
                 const int hv = h - a.Hq - a.Hkv;
-                __nv_bfloat16* dst = a.v_cache + ((page * a.Hkv + hv) * a.page_size + off) * kD;
+                __nv_bfloat16* dst = a.v_cache + kv_slot + hv * (BI_PAGE_SIZE * kD);
                 *reinterpret_cast<uint32_t*>(dst + i0) = lo[j];
                 *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = hi[j];
                 continue;
@@ -119,7 +130,8 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
                 for (int e = 0; e < 4; ++e) ss = __fmaf_rn(x[e], x[e], ss);
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                const float r = rsqrtf(__fdiv_rn(ss, static_cast<float>(kD)) + a.eps);
+                // ss / 128 computed as ss * 2^-7: the same correctly rounded value
+                const float r = rsqrtf(__fmul_rn(ss, 1.f / kD) + a.eps);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     x[e] = __bfloat162float(
@@ -135,7 +147,7 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
             if (is_q) {
                 dst = a.q_out + (static_cast<int64_t>(t) * a.Hq + h) * kD;
             } else {
-                dst = a.k_cache + ((page * a.Hkv + (h - a.Hq)) * a.page_size + off) * kD;
+                dst = a.k_cache + kv_slot + (h - a.Hq) * (BI_PAGE_SIZE * kD);
             }
             *reinterpret_cast<uint32_t*>(dst + i0) = bi::pack_bf16x2(y[0], y[1]);
             *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = bi::pack_bf16x2(y[2], y[3]);
