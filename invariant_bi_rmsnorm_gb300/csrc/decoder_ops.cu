@@ -156,14 +156,14 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
 }
 
 // h[t][j] = bf16( silu(g) * u ),  g = gu[t][j], u = gu[t][F + j],
-// silu(g) = g / (1 + exp(-g)), all in fp32.  8 outputs per thread.
+// silu(g) = g / (1 + exp(-g)), all in fp32.  8 outputs per thread.  The grid
+// is 2-D (vector blocks of a row on x, rows on y) so that no thread divides a
+// flat index by the row length.
 __global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_gu,
                                 __nv_bfloat16* __restrict__ out, int64_t ld_out, int T, int F) {
-    const int64_t nvec = static_cast<int64_t>(T) * (F / 8);
-    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < nvec;
-         v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t t = v / (F / 8);
-        const int j = static_cast<int>(v % (F / 8)) * 8;
+    const int j = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (j >= F) return;
+    for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
         const uint4 gv = *reinterpret_cast<const uint4*>(gu + t * ld_gu + j);
         const uint4 uv = *reinterpret_cast<const uint4*>(gu + t * ld_gu + F + j);
         const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
@@ -224,18 +224,18 @@ extern "C" bi_status bi_qk_norm_rope_append(const void* qkv, int64_t ld_qkv, int
 
 extern "C" bi_status bi_silu_mul(const void* gate_up, int64_t ld_gate_up, int32_t T, int32_t F,
                                  void* out, int64_t ld_out, cudaStream_t stream) {
-    if (T < 0 || F < 8 || (F & 7)) return T < 0 ? BI_ERR_INVALID_ARG : BI_ERR_UNSUPPORTED_SHAPE;
+    if (T < 0 || F < 8 || (F & 7) || F > (1 << 30))
+        return T < 0 ? BI_ERR_INVALID_ARG : BI_ERR_UNSUPPORTED_SHAPE;
     if (ld_gate_up < 2 * static_cast<int64_t>(F) || ld_out < F) return BI_ERR_INVALID_ARG;
     if ((ld_gate_up & 7) || (ld_out & 7)) return BI_ERR_MISALIGNED;
     if (T == 0) return BI_OK;
     if (!gate_up || !out) return BI_ERR_INVALID_ARG;
     if (!bi::aligned16(gate_up) || !bi::aligned16(out)) return BI_ERR_MISALIGNED;
-    const int64_t nvec = static_cast<int64_t>(T) * (F / 8);
     const int threads = 256;
-    const int64_t blocks = std::min<int64_t>((nvec + threads - 1) / threads,
-                                             static_cast<int64_t>(bi::sm_count()) * 16);
-    silu_mul_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), threads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(gate_up), ld_gate_up, static_cast<__nv_bfloat16*>(out),
-        ld_out, T, F);
+    const dim3 grid(static_cast<unsigned>((F / 8 + threads - 1) / threads),
+                    static_cast<unsigned>(std::min(T, 65535)));
+    silu_mul_kernel<<<grid, threads, 0, stream>>>(static_cast<const __nv_bfloat16*>(gate_up),
+                                                   ld_gate_up, static_cast<__nv_bfloat16*>(out),
+                                                   ld_out, T, F);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
