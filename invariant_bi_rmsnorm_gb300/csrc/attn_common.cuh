@@ -94,6 +94,16 @@ __device__ __forceinline__ void page_scores(float (&sc)[4], uint32_t ks_base,
     }
 }
 
+// 2^x by the PTX instruction ex2.approx.ftz.f32 (PTX ISA: maximum relative
+// error 2^-22; subnormal results flushed to zero): one instruction on the
+// per-page dependency chain, where exp2f() takes several. Decode, prefill and
+// the chunk folds all take their exponentials from here.
+__device__ __forceinline__ float exp2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Online-softmax update of one column group from its raw scores: masking,
 // running max, the rescale of l and O, p = 2^(x - m), l += sum p, and p split
 // into bf16 high part + bf16 remainder, transposed into mma B fragments.
@@ -114,12 +124,12 @@ __device__ __forceinline__ void softmax_step(ColState& st, const float (&sc)[4],
     }
     const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
     // a column with no visible token so far keeps m = -inf: no rescale, p = 0
-    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(__fsub_rn(st.m[0], mn0));
-    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(__fsub_rn(st.m[1], mn1));
-    const float p0 = x0 == -INFINITY ? 0.f : exp2f(__fsub_rn(x0, mn0));
-    const float p1 = x1 == -INFINITY ? 0.f : exp2f(__fsub_rn(x1, mn1));
-    const float p2 = x2 == -INFINITY ? 0.f : exp2f(__fsub_rn(x2, mn0));
-    const float p3 = x3 == -INFINITY ? 0.f : exp2f(__fsub_rn(x3, mn1));
+    const float al0 = mn0 == -INFINITY ? 1.f : exp2_ftz(__fsub_rn(st.m[0], mn0));
+    const float al1 = mn1 == -INFINITY ? 1.f : exp2_ftz(__fsub_rn(st.m[1], mn1));
+    const float p0 = x0 == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x0, mn0));
+    const float p1 = x1 == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x1, mn1));
+    const float p2 = x2 == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x2, mn0));
+    const float p3 = x3 == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x3, mn1));
     const uint32_t pA = bi::pack_bf16x2(p0, p1);  // high parts
     const uint32_t pB = bi::pack_bf16x2(p2, p3);
     const uint32_t rA = bi::pack_bf16x2(__fsub_rn(p0, __uint_as_float(pA << 16)),
@@ -192,8 +202,8 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* vd, int valid, int lane) {
 //   l' = fma(l_c, fc, l * fo);  O' = fma(O_c, fc, O * fo).
 __device__ __forceinline__ void fold_scalars(float M, float mc, float& Mn, float& fo, float& fc) {
     Mn = fmaxf(M, mc);
-    fo = exp2f(M - Mn);
-    fc = exp2f(mc - Mn);
+    fo = exp2_ftz(M - Mn);
+    fc = exp2_ftz(mc - Mn);
 }
 
 __device__ __forceinline__ float fold_value(float acc, float fo, float part, float fc) {
