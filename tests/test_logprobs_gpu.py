@@ -68,3 +68,27 @@ def test_masked_vocabulary_entries():
         assert (np.abs(g_ - ref) <= 1e-4 + 1e-6 * np.abs(ref)).all(), np.abs(g_ - ref).max()
     assert abs(lse[3].item() - 1.5) <= 1e-6 and abs(lp[3].item()) <= 1e-6
     bi.get_device_error()
+
+
+def test_terms_below_the_fp32_normal_range():
+    """Each term is one ex2.approx.ftz, which flushes results below 2^-126 to
+    zero.  Rows built so that many terms land there -- every other entry
+    about 100 below the row's maximum (terms near e^-100 = 2^-144), with the
+    maximum first, last, or alone among -inf entries -- must still give the
+    oracle's lse and log-probabilities: a flushed term is far below half an
+    ulp of the sum, which holds the maximum's own term (about 1)."""
+    rows = torch.full((4, V), -100.0)
+    rows[0, 0] = 0.0                       # maximum in the first vector
+    rows[1, V - 1] = 0.0                   # maximum in the last vector, after every tiny term
+    rows[2, 4000:4008] = torch.tensor([-100.0, -99.0, 0.0, -101.0, -98.5, -100.0, -30.0, -97.0])
+    rows[3] = float("-inf")
+    rows[3, 77] = 5.0
+    rows[3, 78] = -95.0                    # one tiny term beside the maximum
+    x = rows.to(torch.bfloat16)
+    t = torch.tensor([0, 5, 4006, 78], dtype=torch.int32)
+    lp, lse = bi.logprobs(x.cuda(), t.cuda())
+    lp_ref, lse_ref = oracle.logprobs(x, t.numpy())
+    for got, ref in ((lp, lp_ref), (lse, lse_ref)):
+        g = got.cpu().double().numpy()
+        assert (np.abs(g - ref) <= 1e-4 + 1e-6 * np.abs(ref)).all(), (g, ref)
+    bi.get_device_error()

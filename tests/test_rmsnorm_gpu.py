@@ -85,6 +85,34 @@ def test_strided_rows_and_in_place():
     assert np.array_equal(bits(xd[:, 4096:]), bits(x[:, 4096:]))  # padding untouched
 
 
+def test_rows_past_the_prefetch_distance_strided():
+    """Each CTA asks L2 for the input row 16 MiB of input ahead of its own (a
+    hint that moves no arithmetic).  At hidden 32768 that is 256 rows ahead
+    (128 for the fused form, which prefetches both inputs), so 600 strided
+    rows cover rows that prefetch, rows near the end that do not, and rows
+    whose prefetched row lies past the end: all within 2 ulp of the oracle and
+    bit-identical to each row computed alone."""
+    Hs, rows, pad = 32768, 600, 64
+    x = inputs.rmsnorm_rows(rows, Hs + pad, seed=31)
+    w = inputs.rmsnorm_weight(Hs, seed=32)
+    xd, wd = x.cuda(), w.cuda()
+    view = xd[:, :Hs]  # leading dimension Hs + 64
+    y = bits(bi.rmsnorm(view, wd, EPS))
+    ref = oracle.round_bf16(oracle.rmsnorm(x[:, :Hs].contiguous(), w, EPS))
+    assert ulp_distance(y, ref).max() <= ULP_TOL
+    for r in (0, 255, 256, 343, 344, 599):
+        one = bits(bi.rmsnorm(view[r:r + 1], wd, EPS))
+        assert np.array_equal(one[0], y[r]), f"row {r}"
+    # the fused residual add + RMSNorm over the same rows
+    res = inputs.rmsnorm_rows(rows, Hs, seed=33).cuda()
+    summed = (res.float() + view.float()).to(torch.bfloat16)
+    want = bits(bi.rmsnorm(summed, wd, EPS))
+    res_out = res.clone()
+    got = bits(bi.add_rmsnorm(view, res_out, wd, EPS))
+    assert np.array_equal(bits(res_out), bits(summed))
+    assert np.array_equal(got, want)
+
+
 def test_special_rows():
     # zero row, constant row, one-hot row, huge and tiny magnitudes (the sum
     # of squares is kept in fp32, so rows stay well inside its range: the
