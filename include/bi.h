@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
     BI_OK = 0,
     BI_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad eps ... */
-    BI_ERR_UNSUPPORTED_SHAPE = 2,  /* a size this build does not handle */
+    BI_ERR_UNSUPPORTED_SHAPE = 2,  /* a size the library does not handle */
     BI_ERR_MISALIGNED = 3,         /* pointer or leading dimension not 16-byte aligned */
     BI_ERR_WORKSPACE_TOO_SMALL = 4,
     BI_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
