@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -347,7 +348,8 @@ __global__ void __launch_bounds__(kD)
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
-bool g_attr_set[64] = {};
+// set once per device; any thread may race to set it, the attribute is idempotent
+std::atomic<bool> g_attr_set[64] = {};
 
 }  // namespace
 

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
@@ -285,7 +286,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     }
 }
 
-bool g_attr_set[2][64] = {};
+// set once per device; any thread may race to set it, the attribute is idempotent
+std::atomic<bool> g_attr_set[2][64] = {};
 
 // Validate and launch.  N is the weight's row count (the accumulator width);
 // the output has N columns, or N/2 for the fused SwiGLU variant.

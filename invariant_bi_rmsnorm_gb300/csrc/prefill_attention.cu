@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "attn_common.cuh"
@@ -244,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-bool g_attr_set[64] = {};
+// set once per device; any thread may race to set it, the attribute is idempotent
+std::atomic<bool> g_attr_set[64] = {};
 
 }  // namespace
 
