@@ -303,6 +303,9 @@ __global__ void __launch_bounds__(kThreads)
 // Fold the chunk partials of one (sequence, query head) in ascending chunk
 // order:  M' = max(M, m_c);  l' = l 2^(M-M') + l_c 2^(m_c-M');
 //         O' = O 2^(M-M') + O_c 2^(m_c-M');   out = bf16(O / l).
+// kBatch: chunks whose partials are loaded before any of them is folded (a
+// schedule choice; the fold stays strictly sequential in c).
+template <int kBatch>
 __global__ void __launch_bounds__(kD)
     attn_merge_kernel(const int32_t* __restrict__ seq_lens, const float* __restrict__ ws_acc,
                       const float* __restrict__ ws_ml, __nv_bfloat16* __restrict__ out, int Hq,
@@ -319,9 +322,6 @@ __global__ void __launch_bounds__(kD)
     float M = ws_ml[base * 2];
     float Ls = ws_ml[base * 2 + 1];
     float A = ws_acc[base * kD + d];
-    // the loads of up to kBatch chunks are issued before any of them is
-    // folded (the fold itself stays strictly sequential in c)
-    constexpr int kBatch = 8;
     for (int cb = 1; cb < nch; cb += kBatch) {
         float mc[kBatch], lc[kBatch], ac[kBatch];
 #pragma unroll
@@ -347,6 +347,11 @@ __global__ void __launch_bounds__(kD)
 }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// (sequence, query head) rows up to which the merge batches 32 chunks' loads:
+// at B = 1 that was 2-3 us faster than 8; at 64 sequences and more it was 2 %
+// slower (more registers, fewer resident CTAs).
+constexpr int64_t kMergeWideRows = 512;
 
 // set once per device; any thread may race to set it, the attribute is idempotent
 std::atomic<bool> g_attr_set[64] = {};
@@ -470,9 +475,16 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     attn_split_kernel<<<dim3(groups, Hkv, B), kThreads, kSmemBytes, stream>>>(tk, tv, args);
     if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
     if (max_chunks > cpc) {
-        attn_merge_kernel<<<dim3(Hq, B), kD, 0, stream>>>(seq_lens, args.ws_acc, args.ws_ml,
-                                                          args.out, Hq, max_chunks, max_seq_len,
-                                                          num_splits, cpc);
+        // few rows: each thread's chain of loads is the bound, so load up to
+        // 32 chunks at once; many rows: 8, for more resident CTAs
+        if (static_cast<int64_t>(B) * Hq <= kMergeWideRows)
+            attn_merge_kernel<32><<<dim3(Hq, B), kD, 0, stream>>>(
+                seq_lens, args.ws_acc, args.ws_ml, args.out, Hq, max_chunks, max_seq_len,
+                num_splits, cpc);
+        else
+            attn_merge_kernel<8><<<dim3(Hq, B), kD, 0, stream>>>(
+                seq_lens, args.ws_acc, args.ws_ml, args.out, Hq, max_chunks, max_seq_len,
+                num_splits, cpc);
         if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
     }
     return BI_OK;
