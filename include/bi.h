@@ -296,7 +296,9 @@ bi_status bi_qk_norm_rope_append(const void* qkv, int64_t ld_qkv, int32_t T, int
 /*
  * bi_silu_mul -- the SwiGLU product: out[t][j] = bf16(silu(g) * u) with
  * g = gate_up[t][j], u = gate_up[t][F + j], silu(g) = g / (1 + exp(-g)), all
- * in fp32.  Pointwise, hence batch-invariant.  F a multiple of 8, at most
+ * in fp32 (exp(-g) as 2^(-g log2 e) by ex2.approx and the quotient as
+ * g * rcp(1 + e) by rcp.approx: a few fp32 ulp, far inside bf16 rounding).
+ * Pointwise, hence batch-invariant.  F a multiple of 8, at most
  * 2^30 (else BI_ERR_UNSUPPORTED_SHAPE).
  *   gate_up  device, bf16 [T][ld_gate_up] (gate columns 0..F-1, up F..2F-1).
  *   out      device, bf16 [T][ld_out].

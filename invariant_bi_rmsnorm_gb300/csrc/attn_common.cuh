@@ -94,15 +94,10 @@ __device__ __forceinline__ void page_scores(float (&sc)[4], uint32_t ks_base,
     }
 }
 
-// 2^x by the PTX instruction ex2.approx.ftz.f32 (PTX ISA: maximum relative
-// error 2^-22; subnormal results flushed to zero): one instruction on the
-// per-page dependency chain, where exp2f() takes several. Decode, prefill and
-// the chunk folds all take their exponentials from here.
-__device__ __forceinline__ float exp2_ftz(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
+// 2^x as one ex2.approx.ftz.f32 (bi::ex2_approx) on the per-page dependency
+// chain, where exp2f() takes several instructions.  Decode, prefill and the
+// chunk folds all take their exponentials from here.
+__device__ __forceinline__ float exp2_ftz(float x) { return bi::ex2_approx(x); }
 
 // Online-softmax update of one column group from its raw scores: masking,
 // running max, the rescale of l and O, p = 2^(x - m), l += sum p, and p split

@@ -39,18 +39,14 @@ __device__ __forceinline__ float rescale(float a, float b) {
     return exp2f(__fmul_rn(__fsub_rn(a, b), kLog2e));
 }
 
-// 2^x by the PTX instruction ex2.approx.ftz.f32 (PTX ISA: maximum relative
-// error 2^-22 over the full range; subnormal results flushed to zero). Used
-// for the per-element terms: it is one instruction where exp2f() takes more,
-// and the kernel is issue-bound as much as it is HBM-bound. A flushed term is
-// below 2^-126. The vector that sets the running maximum also adds that
-// maximum's own term (about 1), so by the end of every vector the sum is near
-// 1 or more, and terms that small round away: the row's (m, s) is unchanged.
-__device__ __forceinline__ float ex2_term(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
+// 2^x as one ex2.approx.ftz.f32 (bi::ex2_approx; subnormal results flushed
+// to zero) for the per-element terms: exp2f() takes about three more
+// instructions, and the kernel is issue-bound as much as it is HBM-bound.  A
+// flushed term is below 2^-126.  The vector that sets the running maximum also
+// adds that maximum's own term (about 1), so by the end of every vector the
+// sum is near 1 or more, and terms that small round away: the row's (m, s) is
+// unchanged.
+__device__ __forceinline__ float ex2_term(float x) { return bi::ex2_approx(x); }
 
 // (m, s) after folding one vector of 8 values in element order; mc = m * c
 __device__ __forceinline__ void fold_vec(float& m, float& mc, float& s, const uint4& u) {
