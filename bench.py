@@ -74,6 +74,8 @@ def parse_args():
     ap.add_argument("--requests", type=int, default=1000, help="--case decoder: requests")
     ap.add_argument("--layers", type=int, default=36, help="--case decoder: decoder layers")
     ap.add_argument("--new-tokens", type=int, default=100, help="--case decoder: tokens per request")
+    ap.add_argument("--budget", type=int, default=8192,
+                    help="--case decoder: tokens per step (decode rows + prompt chunks)")
     ap.add_argument("--track", type=int, default=16,
                     help="--case decoder: requests re-run alone for the bitwise check")
     ap.add_argument("--batch", type=int, default=ATT_B,
@@ -1014,7 +1016,7 @@ def run_decoder(args):
     torch.cuda.set_device(0)
     cfg = qwen3.Qwen3Config(layers=args.layers)
     w = qwen3.Qwen3Weights(cfg, seed=1000)
-    budget = 8192
+    budget = args.budget
 
     def requests():
         return qwen3.random_requests(args.requests, cfg.vocab, 32, 512, args.new_tokens, seed=7)
