@@ -285,6 +285,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  launch_dependents lets
+// the next kernel in the stream be scheduled while this one runs (its CTAs
+// take SMs as they free up and stop in grid_dependency_wait); wait blocks
+// until every prerequisite grid has completed and its memory is visible.  A
+// kernel launched with programmatic serialization must call wait before it
+// touches any global memory an earlier kernel may write or read.
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // 2^x by the PTX instruction ex2.approx.ftz.f32 (PTX ISA: maximum relative
 // error 2^-22 over the full range; subnormal inputs and results flushed to
 // zero).  One instruction.
