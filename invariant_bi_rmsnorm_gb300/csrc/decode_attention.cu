@@ -98,6 +98,8 @@ __device__ __forceinline__ void chunk_geometry(int L, int num_splits, int& ppc, 
 __global__ void __launch_bounds__(kThreads)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     const int cg = blockIdx.x;  // chunk group
     const int g = blockIdx.y;
     const int s = blockIdx.z;
@@ -310,6 +312,8 @@ __global__ void __launch_bounds__(kD)
     attn_merge_kernel(const int32_t* __restrict__ seq_lens, const float* __restrict__ ws_acc,
                       const float* __restrict__ ws_ml, __nv_bfloat16* __restrict__ out, int Hq,
                       int max_chunks, int max_seq_len, int num_splits, int chunks_per_cta) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     const int hq = blockIdx.x;
     const int s = blockIdx.y;
     const int d = threadIdx.x;
@@ -472,20 +476,23 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     }
     args.chunks_per_cta = cpc;
     const int groups = ceil_div(max_chunks, cpc);
-    attn_split_kernel<<<dim3(groups, Hkv, B), kThreads, kSmemBytes, stream>>>(tk, tv, args);
-    if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
+    if (bi::launch_pdl(attn_split_kernel, dim3(groups, Hkv, B), dim3(kThreads), kSmemBytes, stream,
+                       tk, tv, args) != cudaSuccess)
+        return BI_ERR_CUDA;
     if (max_chunks > cpc) {
         // few rows: each thread's chain of loads is the bound, so load up to
         // 32 chunks at once; many rows: 8, for more resident CTAs
-        if (static_cast<int64_t>(B) * Hq <= kMergeWideRows)
-            attn_merge_kernel<32><<<dim3(Hq, B), kD, 0, stream>>>(
-                seq_lens, args.ws_acc, args.ws_ml, args.out, Hq, max_chunks, max_seq_len,
-                num_splits, cpc);
-        else
-            attn_merge_kernel<8><<<dim3(Hq, B), kD, 0, stream>>>(
-                seq_lens, args.ws_acc, args.ws_ml, args.out, Hq, max_chunks, max_seq_len,
-                num_splits, cpc);
-        if (cudaGetLastError() != cudaSuccess) return BI_ERR_CUDA;
+        const cudaError_t e =
+            static_cast<int64_t>(B) * Hq <= kMergeWideRows
+                ? bi::launch_pdl(attn_merge_kernel<32>, dim3(Hq, B), dim3(kD), 0, stream, seq_lens,
+                                 static_cast<const float*>(args.ws_acc),
+                                 static_cast<const float*>(args.ws_ml), args.out, Hq, max_chunks,
+                                 max_seq_len, num_splits, cpc)
+                : bi::launch_pdl(attn_merge_kernel<8>, dim3(Hq, B), dim3(kD), 0, stream, seq_lens,
+                                 static_cast<const float*>(args.ws_acc),
+                                 static_cast<const float*>(args.ws_ml), args.out, Hq, max_chunks,
+                                 max_seq_len, num_splits, cpc);
+        if (e != cudaSuccess) return BI_ERR_CUDA;
     }
     return BI_OK;
 }

@@ -77,6 +77,8 @@ __device__ __forceinline__ void load_heads(const __nv_bfloat16* row, int h0, int
 // six CTAs (48 warps) per SM: capping registers at 40 ran 10 % faster than the
 // natural 61 (four CTAs); at 32 the spills cost more than the extra CTAs gave
 __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel(const RopeArgs a) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -161,6 +163,8 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
 // flat index by the row length.
 __global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_gu,
                                 __nv_bfloat16* __restrict__ out, int64_t ld_out, int T, int F) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     const int j = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (j >= F) return;
     for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
@@ -218,8 +222,10 @@ extern "C" bi_status bi_qk_norm_rope_append(const void* qkv, int64_t ld_qkv, int
     a.num_slots = static_cast<int64_t>(num_pages) * page_size;
     a.page_size = page_size;
     a.err = bi::device_error_word();
-    qk_norm_rope_append_kernel<<<static_cast<unsigned>(T), kRopeWarps * 32, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return bi::launch_pdl(qk_norm_rope_append_kernel, dim3(static_cast<unsigned>(T)),
+                          dim3(kRopeWarps * 32), 0, stream, a) == cudaSuccess
+               ? BI_OK
+               : BI_ERR_CUDA;
 }
 
 extern "C" bi_status bi_silu_mul(const void* gate_up, int64_t ld_gate_up, int32_t T, int32_t F,
@@ -234,8 +240,9 @@ extern "C" bi_status bi_silu_mul(const void* gate_up, int64_t ld_gate_up, int32_
     const int threads = 256;
     const dim3 grid(static_cast<unsigned>((F / 8 + threads - 1) / threads),
                     static_cast<unsigned>(std::min(T, 65535)));
-    silu_mul_kernel<<<grid, threads, 0, stream>>>(static_cast<const __nv_bfloat16*>(gate_up),
-                                                   ld_gate_up, static_cast<__nv_bfloat16*>(out),
-                                                   ld_out, T, F);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return bi::launch_pdl(silu_mul_kernel, grid, dim3(threads), 0, stream,
+                          static_cast<const __nv_bfloat16*>(gate_up), ld_gate_up,
+                          static_cast<__nv_bfloat16*>(out), ld_out, T, F) == cudaSuccess
+               ? BI_OK
+               : BI_ERR_CUDA;
 }

@@ -339,22 +339,11 @@ bi_status launch_gemm(const void* x, const void* W, void* y, int32_t M, int32_t 
     const int64_t budget = int64_t{48} << 20;
     int group_m = num_m;
     if (slab * num_m > budget) group_m = static_cast<int>(std::max<int64_t>(1, budget / slab));
-    // programmatic serialization: this grid may start its set-up while the
-    // previous kernel in the stream finishes (the kernel waits for it before
-    // touching memory)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(pair::kThreads);
-    cfg.dynamicSmemBytes = pair::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemm_tcgen05_pair_kernel<kSwiGLU>, tx, tw,
-                           static_cast<__nv_bfloat16*>(y), M, N, K, ld_y, group_m,
-                           bi::device_error_word()) != cudaSuccess)
+    // programmatic serialization: this grid's set-up may overlap the previous
+    // kernel's tail (the kernel waits for it before touching memory)
+    if (bi::launch_pdl(gemm_tcgen05_pair_kernel<kSwiGLU>, dim3(2 * pairs), dim3(pair::kThreads),
+                       pair::kSmemBytes, stream, tx, tw, static_cast<__nv_bfloat16*>(y), M, N, K,
+                       ld_y, group_m, bi::device_error_word()) != cudaSuccess)
         return BI_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }

@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(kThreads)
     logprobs_kernel(const __nv_bfloat16* __restrict__ logits, int64_t ld, int vocab,
                     const int32_t* __restrict__ targets, float* __restrict__ logprob_out,
                     float* __restrict__ lse_out, uint32_t* err) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
@@ -138,8 +140,9 @@ extern "C" bi_status bi_logprobs(const void* logits, int64_t rows, int32_t vocab
     if (!bi::aligned16(logits) || (reinterpret_cast<uintptr_t>(targets) & 3) ||
         (reinterpret_cast<uintptr_t>(logprob_out) & 3) || (reinterpret_cast<uintptr_t>(lse_out) & 3))
         return BI_ERR_MISALIGNED;
-    logprobs_kernel<<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(logits), ld, vocab, targets, logprob_out, lse_out,
-        bi::device_error_word());
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return bi::launch_pdl(logprobs_kernel, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0,
+                          stream, static_cast<const __nv_bfloat16*>(logits), ld, vocab, targets,
+                          logprob_out, lse_out, bi::device_error_word()) == cudaSuccess
+               ? BI_OK
+               : BI_ERR_CUDA;
 }

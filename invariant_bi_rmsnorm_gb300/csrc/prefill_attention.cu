@@ -71,6 +71,8 @@ __device__ __forceinline__ void consumer_bar_sync() {
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     const int tile = blockIdx.x;
     const int g = blockIdx.y;
     const int s = blockIdx.z;
@@ -310,6 +312,8 @@ extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, co
     args.T = T;
     args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     const int tiles = (max_q_len + args.rows_per_tile - 1) / args.rows_per_tile;
-    prefill_attn_kernel<<<dim3(tiles, Hkv, S), kThreads, kSmemBytes, stream>>>(tk, tv, args);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return bi::launch_pdl(prefill_attn_kernel, dim3(tiles, Hkv, S), dim3(kThreads), kSmemBytes,
+                          stream, tk, tv, args) == cudaSuccess
+               ? BI_OK
+               : BI_ERR_CUDA;
 }

@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kMaxThreads)
     rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloat16* __restrict__ w, __nv_bfloat16* y,
                    int hidden, int64_t ld_x, int64_t ld_y, float eps, __nv_bfloat16* res,
                    int64_t ld_res, int64_t rows, int64_t ahead) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     __shared__ float warp_sums[kMaxThreads / 32];
     const int nvec = hidden >> 3;
     const int tid = threadIdx.x;
@@ -163,17 +165,19 @@ bi_status launch_rmsnorm(const void* x, const void* w, void* y, int64_t rows, in
     auto* yb = static_cast<__nv_bfloat16*>(y);
     auto* rb = static_cast<__nv_bfloat16*>(res);
     const dim3 grid(static_cast<unsigned>(rows));
+    cudaError_t err;
     const int64_t ahead = kPrefetchAheadBytes / (int64_t{hidden} * 2 * (kAdd ? 2 : 1));
     if (vpt == 1)
-        rmsnorm_kernel<1, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
+        err = bi::launch_pdl(rmsnorm_kernel<1, kAdd>, grid, dim3(threads), 0, stream, xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
     else if (vpt == 2)
-        rmsnorm_kernel<2, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
+        err = bi::launch_pdl(rmsnorm_kernel<2, kAdd>, grid, dim3(threads), 0, stream, xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
     else if (vpt <= 4)
-        rmsnorm_kernel<4, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
+        err = bi::launch_pdl(rmsnorm_kernel<4, kAdd>, grid, dim3(threads), 0, stream, xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
     else if (vpt <= 8)
-        rmsnorm_kernel<8, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
+        err = bi::launch_pdl(rmsnorm_kernel<8, kAdd>, grid, dim3(threads), 0, stream, xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
     else
-        rmsnorm_kernel<16, kAdd><<<grid, threads, 0, stream>>>(xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
+        err = bi::launch_pdl(rmsnorm_kernel<16, kAdd>, grid, dim3(threads), 0, stream, xb, wb, yb, hidden, ld_x, ld_y, eps, rb, ld_res, rows, ahead);
+    if (err != cudaSuccess) return BI_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
