@@ -5,7 +5,11 @@
  * a CUDA stream; none allocates memory, keeps per-call state, or synchronises
  * the stream (except bi_get_device_error).  All launches are asynchronous on
  * `stream`.  Arguments are validated on the host before anything is launched:
- * an invalid call returns an error status and launches nothing.
+ * an invalid call returns an error status and launches nothing.  Kernels are
+ * launched with programmatic stream serialization: a kernel may be scheduled,
+ * and do its set-up, while the previous kernel on the stream finishes, but it
+ * waits for that kernel to complete before it reads or writes global memory,
+ * so stream order holds as for any launch.
  *
  * The property every kernel here guarantees ("batch invariance", after
  * "Defeating Nondeterminism in LLM Inference: The Core Role of Batch
