@@ -66,12 +66,14 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the cold-L2 timings of the kernels beyond the bench step")
+    ap.add_argument("--no-c5", action="store_true",
+                    help="skip the C5 decoder run (36 layers, 1000 requests) of the default line")
     ap.add_argument("--case", choices=["gemm_gate_up", "gemm_qkv", "gemm_layers", "attention",
                                        "rmsnorm", "decoder", "prefill", "add_rmsnorm",
                                        "logprobs", "qk_norm_rope_append", "silu_mul",
                                        "gemm_swiglu", "decode_latency"],
                     help="time one kernel of the path alone (for profiling); prints its own line")
-    ap.add_argument("--requests", type=int, default=1000, help="--case decoder: requests")
+    ap.add_argument("--requests", type=int, default=1000, help="C5 decoder (--case decoder and the default line): requests")
     ap.add_argument("--layers", type=int, default=36, help="--case decoder: decoder layers")
     ap.add_argument("--new-tokens", type=int, default=100, help="--case decoder: tokens per request")
     ap.add_argument("--budget", type=int, default=8192,
@@ -255,7 +257,7 @@ class Workload:
         p = inputs.decode_problem(ATT_B, Hq=HQ, Hkv=HKV, D=HD, max_len=MAX_LEN, seed=270, device=dev)
         self.att = {k: v.to(dev) for k, v in p.items()}
         self.att_out = torch.empty(ATT_B, HQ, HD, dtype=torch.bfloat16, device=dev)
-        self.ws = torch.empty(bi.decode_attention_workspace_size(ATT_B, HQ, HD, MAX_LEN),
+        self.ws = torch.zeros(bi.decode_attention_workspace_size(ATT_B, HQ, HD, MAX_LEN),
                               dtype=torch.uint8, device=dev)
         lens = p["seq_lens"].to(torch.int64)
         self.att_lens = lens
@@ -359,7 +361,7 @@ class Workload:
                 q, a["k_cache"], a["v_cache"], bt, sl, max_seq_len=MAX_LEN, out=out,
                 workspace=self.ws), reps, flush)
             ns = max(1, min(32, -(-2 * 152 // (B * HKV))))
-            ws = torch.empty(self.bi.decode_attention_workspace_size(B, HQ, HD, ns * 256),
+            ws = torch.zeros(self.bi.decode_attention_workspace_size(B, HQ, HD, ns * 256),
                              dtype=torch.uint8, device=self.dev)
             t_fc = time_cold(lambda: self.bi.decode_attention_fixed_splits(
                 q, a["k_cache"], a["v_cache"], bt, sl, MAX_LEN, ns, out=out, workspace=ws),
@@ -368,7 +370,9 @@ class Workload:
                             "frac_of_measured_hbm": round(nbytes / t / 1e6 / hbm, 4),
                             "kv_tokens": int(lens.sum()),
                             "fixed_split_count": ns, "fixed_split_count_ms": round(t_fc, 4),
-                            "cost_vs_fixed_split_count": round(t / t_fc, 4)}
+                            "cost_vs_fixed_split_count": round(t / t_fc, 4),
+                            "launches": int(self.bi._lib.load().bi_decode_attention_launches(
+                                B, HKV, MAX_LEN))}
         res["bi_decode_attention_by_batch"] = by_b
         for name in NEXT_CASES:
             fn, work, unit, info = build_next_case(name, self.dev, self.bi, inputs)
@@ -441,7 +445,7 @@ class Workload:
         # count a split-KV kernel would pick to fill 152 SMs at this batch
         ns = max(1, min(32, -(-2 * 152 // (ATT_B * HKV))))
         a = self.att
-        ws_fc = torch.empty(self.bi.decode_attention_workspace_size(ATT_B, HQ, HD, ns * 256),
+        ws_fc = torch.zeros(self.bi.decode_attention_workspace_size(ATT_B, HQ, HD, ns * 256),
                             dtype=torch.uint8, device=self.dev)
         t = timeit(lambda: self.bi.decode_attention_fixed_splits(
             a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"], MAX_LEN, ns,
@@ -529,6 +533,11 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(wl, args, dev, barrier, dist, world)
+    c5 = None
+    if world == 1 and not args.no_c5:
+        # the end-to-end C5 run, after every timed region of the line
+        torch.cuda.empty_cache()
+        c5 = decoder_c5(args.requests, args.layers, args.new_tokens, args.budget, args.track)
 
     if rank != 0:
         if dist is not None:
@@ -585,7 +594,14 @@ def run_ours(args):
                 "torch_rms_norm_gbs_same_run": round(refs.get("torch_rms_norm_gbs", float("nan")), 1),
                 "traffic": traffic_record("bi_rmsnorm")},
         },
-        "bitwise_invariant": all(invariant.values()),
+        # the components' headline fractions, repeated at the top level
+        "cost_vs_cublas": round(refs["cublas_tflops"] / per_gpu_gemm, 4),
+        "attention_frac_of_measured_hbm": round(att_gbs / world / hbm, 4),
+        "rmsnorm_frac_of_measured_hbm": round(rms_gbs / world / hbm, 4),
+        **({"attention_small_batch_frac_of_measured_hbm": {
+            b: extra["bi_decode_attention_by_batch"][b]["frac_of_measured_hbm"]
+            for b in ("1", "16")}} if extra is not None else {}),
+        "bitwise_invariant": all(invariant.values()) and (c5 is None or c5["bitwise_invariant"]),
         **({"next_rows": extra} if extra is not None else {}),
         "invariance_checks": invariant,
         "negative_controls": controls,
@@ -596,6 +612,8 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if c5 is not None:
+        line["c5"] = c5
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)
@@ -891,7 +909,8 @@ def build_next_case(name: str, dev, bi, inputs):
         g = torch.Generator().manual_seed(631)
         pos = torch.randint(0, 8192, (T,), generator=g, dtype=torch.int64).to(torch.int32).to(dev)
         slots = torch.randperm(npages * 16, generator=g).to(torch.int32).to(dev)
-        rope = bi.rope_table(8192, 1e6, HD, device=dev)
+        from invariant_bi_rmsnorm_gb300.qwen3 import rope_table
+        rope = rope_table(8192, 1e6, HD, device=dev)
         ones = torch.ones(HD, dtype=torch.bfloat16, device=dev)
         qo = torch.empty(T, HQ, HD, dtype=torch.bfloat16, device=dev)
         fn = lambda: bi.qk_norm_rope_append(qkv, HQ, HKV, pos, slots, rope, ones, ones,  # noqa: E731
@@ -973,7 +992,7 @@ def run_case(args):
         p = inputs.decode_problem(B, max_len=MAX_LEN, seed=270, device=dev)
         a = {k: v.to(dev) for k, v in p.items()}
         out = torch.empty(B, HQ, HD, dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(bi.decode_attention_workspace_size(B, HQ, HD, MAX_LEN),
+        ws = torch.zeros(bi.decode_attention_workspace_size(B, HQ, HD, MAX_LEN),
                          dtype=torch.uint8, device=dev)
         lens = p["seq_lens"].to(torch.int64)
         work = float((lens * HKV * HD * 4).sum() + B * HQ * HD * 4 + 4 * ((lens + 15) // 16).sum())
@@ -1001,65 +1020,80 @@ def run_case(args):
                       "value": round(work / (ms * 1e-3) / scale, 2), "unit": unit}), flush=True)
 
 
-def run_decoder(args):
+TORCH_ARM_SWAPS = ("GEMMs -> torch.matmul (cuBLAS, unfused gate|up then bi_silu_mul) and RMSNorms "
+                   "-> torch.nn.functional.rms_norm; attention, q/k norm + RoPE + KV append and "
+                   "SwiGLU stay on this library, so the bi arm's fused gate|up+SwiGLU GEMM is "
+                   "part of the wall-time difference, not only the cost of invariance")
+
+
+def decoder_c5(requests: int = 1000, layers: int = 36, new_tokens: int = 100,
+               budget: int = 8192, track: int = 16) -> dict:
     """The random-init Qwen3-8B-shaped decoder served with continuous batching:
     `requests` prompts of U[32, 512] random tokens, `new_tokens` greedy tokens
-    each, at most 8192 tokens per step (prompts split across steps as needed).
-    Timed: the whole batched run (wall clock, host scheduling included).  Then
-    `track` requests are re-run alone and their logits compared bit for bit
-    with the batched run at every generated token; the same batched run with
-    torch/cuBLAS GEMMs and torch RMSNorms swapped in is timed and checked the
-    same way, as the non-invariant comparison."""
+    each, at most `budget` tokens per step (prompts split across steps as
+    needed).  Timed: the whole batched run (wall clock, host scheduling
+    included).  Then `track` requests are re-run alone and their logits
+    compared bit for bit with the batched run at every generated token; the
+    same batched run with torch/cuBLAS GEMMs and torch RMSNorms swapped in is
+    timed and checked the same way, as the non-invariant comparison."""
     import __graft_entry__
     from invariant_bi_rmsnorm_gb300 import qwen3
     __graft_entry__.build()
-    torch.cuda.set_device(0)
-    cfg = qwen3.Qwen3Config(layers=args.layers)
+    cfg = qwen3.Qwen3Config(layers=layers)
     w = qwen3.Qwen3Weights(cfg, seed=1000)
-    budget = args.budget
 
-    def requests():
-        return qwen3.random_requests(args.requests, cfg.vocab, 32, 512, args.new_tokens, seed=7)
+    def make_requests():
+        return qwen3.random_requests(requests, cfg.vocab, 32, 512, new_tokens, seed=7)
 
-    reqs = requests()
-    pages = sum(-(-(len(r.prompt) + args.new_tokens) // 16) for r in reqs) + 64
-    track = sorted({int(i) for i in np.linspace(0, args.requests - 1, args.track)})
-    result = {"case": "decoder", "requests": args.requests, "layers": args.layers,
-              "prompt_len": "U[32,512]", "new_tokens": args.new_tokens,
+    reqs = make_requests()
+    pages = sum(-(-(len(r.prompt) + new_tokens) // 16) for r in reqs) + 64
+    tracked = sorted({int(i) for i in np.linspace(0, requests - 1, track)})
+    result = {"requests": requests, "layers": layers,
+              "prompt_len": "U[32,512]", "new_tokens": new_tokens,
               "max_tokens_per_step": budget, "model": "random-init Qwen3-8B-shaped "
               "(hidden 4096, FFN 12288, 32/8 heads, d128, vocab 151936, RoPE 1e6)",
-              "prompt_tokens": int(sum(len(r.prompt) for r in reqs))}
+              "prompt_tokens": int(sum(len(r.prompt) for r in reqs)),
+              "torch_arm_swaps": TORCH_ARM_SWAPS}
     for ops in ("bi", "torch"):
         eng = qwen3.Engine(w, num_pages=pages, max_tokens_per_step=budget, ops=ops)
         warm = qwen3.random_requests(4, cfg.vocab, 32, 64, 2, seed=99)
         eng.generate(warm)
         eng.reset()
-        reqs = requests()
+        reqs = make_requests()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        logs = eng.generate(reqs, record=set(track))
+        logs = eng.generate(reqs, record=set(tracked))
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         steps = eng.steps
         mism_logits = mism_tokens = 0
-        for sid in track:
+        for sid in tracked:
             eng.reset()
-            one = qwen3.Sequence(sid=sid, prompt=list(reqs[sid].prompt), max_new=args.new_tokens)
+            one = qwen3.Sequence(sid=sid, prompt=list(reqs[sid].prompt), max_new=new_tokens)
             alone = eng.generate([one], record={sid})
             mism_tokens += int(one.generated != reqs[sid].generated)
             mism_logits += sum(int(not torch.equal(a, b)) for a, b in zip(alone[sid], logs[sid]))
-        toks = result["prompt_tokens"] + args.requests * args.new_tokens
+        toks = result["prompt_tokens"] + requests * new_tokens
         result[ops] = {"wall_s": round(wall, 3), "steps": steps,
                        "tokens_per_s": round(toks / wall, 1),
-                       "tracked_requests": len(track),
-                       "logit_rows_compared": len(track) * args.new_tokens,
+                       "tracked_requests": len(tracked),
+                       "logit_rows_compared": len(tracked) * new_tokens,
                        "logit_rows_differing_alone_vs_batched": mism_logits,
                        "requests_whose_tokens_differ": mism_tokens}
         del eng
         torch.cuda.empty_cache()
+    del w
+    torch.cuda.empty_cache()
     result["bitwise_invariant"] = result["bi"]["logit_rows_differing_alone_vs_batched"] == 0
     result["cost_vs_torch_ops"] = round(result["bi"]["wall_s"] / result["torch"]["wall_s"], 4)
-    print(json.dumps(result), flush=True)
+    return result
+
+
+def run_decoder(args):
+    """`--case decoder`: the C5 decoder run alone, its own JSON line."""
+    torch.cuda.set_device(0)
+    res = decoder_c5(args.requests, args.layers, args.new_tokens, args.budget, args.track)
+    print(json.dumps({"case": "decoder", **res}), flush=True)
 
 
 def run_decode_latency(args):

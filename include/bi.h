@@ -37,12 +37,14 @@
 extern "C" {
 #endif
 
-#define BI_ABI_VERSION 1
+#define BI_ABI_VERSION 2
 
 /* Tokens per KV-cache page and per attention split.  Both are fixed: the
  * split size is part of the arithmetic (see bi_decode_attention). */
 #define BI_PAGE_SIZE 16
 #define BI_DECODE_CHUNK 256
+/* Bytes of arrival counters at the start of a decode-attention workspace. */
+#define BI_DECODE_COUNTER_BYTES 262144
 
 typedef enum {
     BI_OK = 0,
@@ -163,9 +165,10 @@ bi_status bi_gemm_swiglu(const void* x, const void* W_gu, void* h, int32_t M, in
 
 /*
  * Workspace bytes bi_decode_attention needs for B sequences of at most
- * max_seq_len tokens with Hq query heads of size D: one fp32 partial
- * (max, sum, D-vector) per (sequence, query head, 256-token chunk).
- * Returns 0 for invalid arguments.
+ * max_seq_len tokens with Hq query heads of size D: BI_DECODE_COUNTER_BYTES of
+ * arrival counters, then one fp32 partial (max, sum, D-vector) per (sequence,
+ * query head, 256-token chunk).  0 when max_seq_len <= 256 (no sequence has a
+ * second chunk, nothing is written) and for invalid arguments.
  */
 size_t bi_decode_attention_workspace_size(int32_t B, int32_t Hq, int32_t D, int32_t max_seq_len);
 
@@ -184,10 +187,13 @@ int32_t bi_decode_chunk_len(int32_t seq_len, int32_t c);
  * Operation: "3. Batch-Invariant Attention" of the same page, with the fixed
  * split-SIZE strategy ("Fixed Size Split KV Strategy"; "Batch Invariance and
  * Numerical Reproducibility": 1000 tokens = 3 x 256 + 232).  Each sequence's
- * keys are cut into consecutive 256-token chunks; one CTA computes each
+ * keys are cut into consecutive 256-token chunks; one warp computes each
  * chunk's partial (running max, sum of exponentials, unnormalised output)
  * with an online softmax over its 16 pages in a fixed order; the partials are
- * then folded in ascending chunk order with the log-sum-exp rule.  The
+ * then folded in ascending chunk order with the log-sum-exp rule, by the CTA
+ * that holds all of a sequence's chunks or else by the last of its CTAs to
+ * finish (an integer arrival counter, no float atomics).  One kernel launch
+ * (two only when B * Hkv > BI_DECODE_COUNTER_BYTES / 4).  The
  * arithmetic for a sequence depends only on its own length and data, never on
  * B, on other sequences, or on tokens stored past seq_lens[s].  The cache is
  * read only: the caller writes the current token's K/V into its page slot
@@ -211,10 +217,18 @@ int32_t bi_decode_chunk_len(int32_t seq_len, int32_t c);
  *   out          device, bf16 [B][Hq][D].
  *   workspace    device, >= bi_decode_attention_workspace_size(B, Hq, D,
  *                max_seq_len) bytes, 16-byte aligned; may be null when that
- *                size is 0.  After the call it holds, for every sequence with
- *                more than one chunk, the fp32 chunk partials in the layout
- *                [B][Hq][chunks][D] (unnormalised outputs) followed by
- *                [B][Hq][chunks][2] (max in log2 units of scale*q.k, sum).
+ *                size is 0.  Its first BI_DECODE_COUNTER_BYTES are uint32
+ *                arrival counters that MUST BE ZERO when the workspace is
+ *                first used (allocate it zero-filled, or clear those bytes
+ *                once); every call leaves them zero again, also a call that
+ *                reports a device error, so a workspace can serve any later
+ *                call without clearing.  Do not share one workspace between
+ *                calls that may run at the same time.  After the counters the
+ *                call leaves, for every sequence with more than one chunk,
+ *                the fp32 chunk partials in the layout [B][Hq][chunks][D]
+ *                (unnormalised outputs) followed by [B][Hq][chunks][2] (max
+ *                in log2 units of scale*q.k, sum), chunks =
+ *                ceil(max_seq_len / 256).
  * Pointers to bf16 data must be 16-byte aligned, int32 arrays 4-byte aligned.
  * Host-side errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED,
  * WORKSPACE_TOO_SMALL, CUDA.  A seq_lens entry outside 1 .. max_seq_len or a
@@ -357,9 +371,11 @@ bi_status bi_decode_attention_fixed_splits(const void* q, const void* k_cache,
                                            cudaStream_t stream);
 
 /* Kernel launches one bi_decode_attention call makes on the current device:
- * 1 when every sequence's chunks are folded inside its CTA, 2 when the merge
- * kernel runs too.  A schedule detail -- the results are the same bits either
- * way.  0 for invalid arguments or when no device is available. */
+ * 1 whenever B * Hkv <= BI_DECODE_COUNTER_BYTES / 4 (each sequence is folded
+ * by its own CTA or by the last of its CTAs to arrive), else 2 when some
+ * sequence spans several CTAs (the separate merge kernel folds it).  A
+ * schedule detail -- the results are the same bits either way.  0 for
+ * invalid arguments or when no device is available. */
 int32_t bi_decode_attention_launches(int32_t B, int32_t Hkv, int32_t max_seq_len);
 
 /*
@@ -378,20 +394,27 @@ int32_t bi_decode_attention_launches(int32_t B, int32_t Hkv, int32_t max_seq_len
  * entry point; it exists only for those callers.
  *
  * Limits and behaviour:
- *   - the scratch holds 65536 chunk partials: B * Hq * ceil(max_seq_len/256)
- *     must not exceed 65536 (for example 64 sequences of 32 heads up to 8192
- *     tokens, or 256 sequences of 32 heads up to 2048 tokens); larger calls
- *     return BI_ERR_WORKSPACE_TOO_SMALL and launch nothing.
- *   - the array takes 32.5 MiB of device memory on every GPU that loads the
+ *   - the scratch holds 65536 chunk partials: when max_seq_len > 256,
+ *     B * Hq * ceil(max_seq_len/256) must not exceed 65536 (for example 64
+ *     sequences of 32 heads up to 8192 tokens, or 256 sequences of 32 heads
+ *     up to 2048 tokens); larger calls return BI_ERR_WORKSPACE_TOO_SMALL and
+ *     launch nothing.  With max_seq_len <= 256 nothing is written to the
+ *     scratch and any B up to 65535 is accepted.
+ *   - the array takes 32.75 MiB of device memory on every GPU that loads the
  *     library, for as long as the library stays loaded.
  *   - nothing is allocated or freed: no cudaMalloc, no cudaFree, no library
- *     allocator.  The first call on each device looks up the array's device
- *     address (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture.
- *   - every call on a device shares the one array and it keeps the last
- *     call's partials; nothing in it needs to start at zero.  Calls whose
- *     kernels may overlap on the GPU (different streams, without ordering
- *     between them) race on it and must be serialised by the caller.
+ *     allocator.  The first call on each device that needs the scratch looks
+ *     up the array's device address (cudaGetSymbolAddress) and caches it for
+ *     the life of the process; make that first call before any stream
+ *     capture (made during a capture, it returns BI_ERR_CUDA).  A
+ *     cudaDeviceReset discards the array and the cached address with it:
+ *     do not call this entry point on a device after resetting it.
+ *   - every call on a device shares the one array: its arrival counters
+ *     start at zero when the library loads and every call leaves them zero;
+ *     the partials keep the last call's values and need no clearing.  Calls
+ *     whose kernels may overlap on the GPU (different streams, without
+ *     ordering between them) race on it and must be serialised by the
+ *     caller.
  * Other arguments, errors and device-side checks: as bi_decode_attention.
  */
 bi_status bi_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,

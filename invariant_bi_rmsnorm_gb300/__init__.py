@@ -26,12 +26,12 @@ import math
 import torch
 
 from . import _lib
-from ._lib import DECODE_CHUNK, PAGE_SIZE
+from ._lib import DECODE_CHUNK, DECODE_COUNTER_BYTES, PAGE_SIZE
 
 __all__ = ["BiError", "rmsnorm", "gemm", "gemm_swiglu", "interleave_gate_up",
            "decode_attention", "decode_attention_fixed_splits",
            "prefill_attention", "add_rmsnorm", "qk_norm_rope_append", "silu_mul",
-           "rope_table", "logprobs",
+           "logprobs",
            "decode_attention_workspace_size", "selftest_wait_timeout",
            "decode_num_chunks", "decode_chunk_len", "get_device_error", "abi_version",
            "status_string", "PAGE_SIZE", "DECODE_CHUNK"]
@@ -127,18 +127,6 @@ def add_rmsnorm(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: f
                                       _row_major_2d(out, "out"), float(eps), _stream(stream)),
            "bi_add_rmsnorm")
     return out
-
-
-def rope_table(max_pos: int, theta: float, D: int = 128, device=None) -> torch.Tensor:
-    """fp32 [max_pos][D] table: cos(pos * f_i) at i and sin(pos * f_i) at D/2 + i,
-    f_i = theta^(-i/(D/2)), evaluated in float64 on the host and rounded once."""
-    half = D // 2
-    pos = torch.arange(max_pos, dtype=torch.float64)[:, None]
-    f = torch.pow(torch.tensor(float(theta), dtype=torch.float64),
-                  -torch.arange(half, dtype=torch.float64) / half)[None, :]
-    ang = pos * f
-    tab = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
-    return tab.to(device) if device is not None else tab
 
 
 def qk_norm_rope_append(qkv: torch.Tensor, Hq: int, Hkv: int, positions: torch.Tensor,
@@ -307,7 +295,9 @@ def decode_attention_fixed_splits(q, k_cache, v_cache, block_table, seq_lens, ma
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
     need = decode_attention_workspace_size(B, Hq, D, int(num_splits) * DECODE_CHUNK)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        # the leading arrival counters must start at zero (every call leaves
+        # them zero, so a caller-kept workspace is cleared only once)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(_lib.load().bi_decode_attention_fixed_splits(
@@ -390,7 +380,9 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         raise ValueError("decode_attention: out must be a contiguous [B, Hq, D] tensor")
     need = decode_attention_workspace_size(B, Hq, D, max_seq_len)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        # the leading arrival counters must start at zero (every call leaves
+        # them zero, so a caller-kept workspace is cleared only once)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(_lib.load().bi_decode_attention(

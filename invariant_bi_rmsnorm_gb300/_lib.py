@@ -22,6 +22,7 @@ BI_ERR_DEVICE_BAD_INPUT = 7
 
 PAGE_SIZE = 16
 DECODE_CHUNK = 256
+DECODE_COUNTER_BYTES = 262144  # arrival counters at the start of an attention workspace
 
 # every entry point include/bi.h declares
 EXPORTS = (

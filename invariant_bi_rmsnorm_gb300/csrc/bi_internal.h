@@ -14,6 +14,10 @@ namespace bi {
 // the clock does not advance.
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kWaitPollLimit = 1u << 28;
+// After a wait has timed out, a kernel gives each copy or MMA it issued and
+// never saw complete this much more time before it exits (its shared memory
+// and TMEM must not be released under an operation still in flight).
+constexpr uint64_t kDrainNs = 20000000ull;
 
 // Device error word values (low byte = bi_status, next byte = where).
 enum : uint32_t {

@@ -245,6 +245,29 @@ __device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t
         : "memory");
 }
 
+// Integer add at device scope with acquire-release semantics; returns the old
+// value.  After a CTA barrier, one thread's release publishes the whole CTA's
+// earlier writes; its acquire, followed by a CTA barrier, lets every thread
+// of the CTA read what the other releasing CTAs published.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// 16 bytes global -> shared, asynchronously, through L2 only (cp.async.cg),
+// and the wait for this thread's outstanding copies.
+__device__ __forceinline__ void cp_async_16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)),
+                 "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------- warp-level mma.sync ----
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                             uint32_t& r2, uint32_t& r3) {

@@ -18,11 +18,16 @@
 // warp.  A chunk's final state is its
 // partial (m, l, O).  If the CTA's group holds every chunk of the sequence,
 // the partials are folded in ascending chunk order inside the CTA (warp by
-// warp after each round of four chunks) and bf16(O / l) is written; otherwise
-// the partials go to the workspace.
-// Kernel 2 (merge): for each (sequence, query head) not finished by one CTA,
-// fold the partials in ascending chunk order -- the same fp32 operations in
-// the same order -- and write bf16(O / l).
+// warp after each round of four chunks) and bf16(O / l) is written.
+// Otherwise the CTA writes its chunks' partials to the workspace and counts
+// itself in on an integer arrival counter of its (sequence, kv-head); the CTA
+// that arrives last reads every chunk's partial back and folds them in
+// ascending chunk order -- the same fp32 operations in the same order -- then
+// writes bf16(O / l) and returns the counter to zero.  Which CTA arrives last
+// decides only who folds, never what is folded or in which order.  No float
+// atomics: the counter is a plain integer add.
+// Kernel 2 (merge), only for launches with more (sequence, kv-head) pairs
+// than the workspace has counters: the same fold as a separate kernel.
 // How many chunks a CTA walks is chosen per launch to fill the GPU; it moves
 // work between CTAs but never changes any operation or its order, so it
 // cannot change a bit of the result.
@@ -64,6 +69,12 @@ constexpr int kSPW = 2;
 constexpr int kStages = kWarps * kSPW;
 constexpr int kSmemBytes = kStages * kStageBytes + kFoldFloats * 4 + 4 * kMaxPagesPerCta +
                            8 * kStages + 1024 /*align*/;
+// Arrival counters at the start of the workspace: one uint32 per (sequence,
+// kv-head), low 16 bits = CTAs arrived, high bits set by a CTA that found a bad
+// page index.  Every call leaves them zero.
+constexpr int64_t kMaxCounters = BI_DECODE_COUNTER_BYTES / 4;
+constexpr uint32_t kArrive = 1u;
+constexpr uint32_t kArriveBad = 0x10001u;
 
 struct SplitArgs {
     const __nv_bfloat16* q;
@@ -72,6 +83,7 @@ struct SplitArgs {
     __nv_bfloat16* out;
     float* ws_acc;  // [B][Hq][max_chunks][D]
     float* ws_ml;   // [B][Hq][max_chunks][2]
+    uint32_t* counters;  // [B][Hkv] arrival counters; nullptr: the merge kernel folds
     uint32_t* err;
     int max_pages_per_seq;
     int Hq, Hkv, group;
@@ -93,6 +105,155 @@ __device__ __forceinline__ void chunk_geometry(int L, int num_splits, int& ppc, 
     const int npg = (L + kPage - 1) / kPage;
     ppc = num_splits > 0 ? (npg + num_splits - 1) / num_splits : kPagesPerChunk;
     nch = (npg + ppc - 1) / ppc;
+}
+
+// The fold of one (sequence, kv-head) by the CTA that arrived last: for each
+// of its G query heads h and dims d (thread d), the chunk partials are folded
+// in ascending chunk order,
+//     M' = max(M, m_c);  fo = 2^(M - M');  fc = 2^(m_c - M');
+//     l' = fma(l_c, fc, l * fo);  O' = fma(O_c, fc, O * fo),
+// starting from chunk 0's (m, l, O), and bf16(O / l) is written -- exactly the
+// merge kernel's operations, on the same values.  Only the schedule differs:
+//   - the running maxima M are a prefix maximum, exact in any evaluation
+//     order, so a warp computes them for 32 chunks at once by a shuffle scan,
+//     and with them every chunk's factors fo, fc;
+//   - the recurrences of l and O then run in every thread from shared
+//     memory, loads issued a few chunks ahead (each thread computes its
+//     heads' l itself, the same operations on the same values).
+// The partials are staged in shared memory (the TMA ring, free by now) a
+// batch of chunks at a time: the (m, l) pairs first, then the unnormalised
+// outputs by cp.async while the factors are computed.  ws reads go through L2
+// only (ld.cg, cp.async.cg): the data was written by other CTAs.
+template <int G>
+__device__ __forceinline__ void fold_sequence(const SplitArgs& a, int s, int g, int nch,
+                                              uint8_t* stage, float* small, int tid) {
+    constexpr int kcb = (kStages * kStageBytes) / (G * kD * 4);  // chunks per batch, G*kcb <= 128
+    // thread -> (head, G consecutive dims) when G divides 128 (vector loads,
+    // one head per warp at G = 4); otherwise thread d -> dim d of every head
+    constexpr bool kVec = kThreads % G == 0 && kD == kThreads;  // G = 1, 2, 4, 8
+    constexpr int TPH = kVec ? kThreads / G : kThreads;  // threads per head
+    constexpr int NH = kVec ? 1 : G;                     // heads per thread
+    constexpr int ND = kVec ? G : 1;                     // dims per thread
+    constexpr int U = kVec ? 4 : (16 / G > 0 ? 16 / G : 1);  // chunks loaded ahead
+    float* acc_s = reinterpret_cast<float*>(stage);  // [kcb][G][kD]
+    float* ml_s = small;                             // [kcb][G][2]  (m_c, l_c)
+    float4* fl = reinterpret_cast<float4*>(small + 256);  // [kcb][G]  (fo, fc, l_c, -)
+    float* mcarry = small + 768;                     // [G] running max before the batch
+    const int lane = tid & 31, warp = tid >> 5;
+    const int64_t row0 = static_cast<int64_t>(s) * a.Hq + g * G;
+    const int h0 = kVec ? tid / TPH : 0;               // this thread's (first) head
+    const int d0 = kVec ? (tid % TPH) * ND : tid;      // this thread's first dim
+    float A[NH][ND], Lr[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+        Lr[j] = 0.f;
+#pragma unroll
+        for (int e = 0; e < ND; ++e) A[j][e] = 0.f;
+    }
+    for (int cb = 0; cb < nch; cb += kcb) {
+        const int nb = min(kcb, nch - cb);
+        float2 ml = make_float2(0.f, 0.f);  // one (m, l) pair per thread (nb * G <= 128)
+        const int mi = tid / G, mh = tid - mi * G;
+        if (mi < nb)
+            ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + ((row0 + mh) * a.max_chunks + cb + mi) * 2));
+        for (int idx = tid; idx < nb * G * (kD / 4); idx += kThreads) {
+            const int v = idx % (kD / 4);
+            const int hg = idx / (kD / 4);  // i * G + h
+            const int i = hg / G, h = hg - i * G;
+            bi::cp_async_16(acc_s + hg * kD + 4 * v,
+                            a.ws_acc + ((row0 + h) * a.max_chunks + cb + i) * kD + 4 * v);
+        }
+        if (mi < nb) *reinterpret_cast<float2*>(ml_s + 2 * tid) = ml;
+        __syncthreads();  // (m, l) staged; the outputs may still be in flight
+        for (int h = warp; h < G; h += kWarps) {
+            float carry = cb == 0 ? -INFINITY : mcarry[h];
+            for (int j0 = 0; j0 < nb; j0 += 32) {
+                const int i = j0 + lane;
+                const int k = i * G + h;
+                const float mc = i < nb ? ml_s[2 * k] : -INFINITY;
+                float v = mc;  // inclusive prefix maximum over the lanes
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v = fmaxf(v, o);
+                }
+                // running max after chunk cb + i (chunk 0 starts the run)
+                const float Mn = cb + j0 == 0 ? v : fmaxf(carry, v);
+                float Mo = __shfl_up_sync(0xffffffffu, Mn, 1);
+                if (lane == 0) Mo = carry;
+                if (i < nb) {
+                    const bool first = cb + i == 0;  // chunk 0: no factors
+                    fl[k] = make_float4(first ? 0.f : bi_attn::exp2_ftz(Mo - Mn),
+                                        first ? 0.f : bi_attn::exp2_ftz(mc - Mn), ml_s[2 * k + 1], 0.f);
+                }
+                carry = __shfl_sync(0xffffffffu, Mn, 31);
+            }
+            __syncwarp();
+            if (lane == 0) mcarry[h] = carry;
+        }
+        bi::cp_async_wait_all();
+        __syncthreads();  // factors and outputs staged
+        for (int i0 = 0; i0 < nb; i0 += U) {
+            float x[U][NH][ND];
+            float4 f[U][NH];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    const int k = (i0 + u) * G + h0 + j;
+                    if (i0 + u < nb) {
+                        f[u][j] = fl[k];
+                        const float* xs = acc_s + k * kD + d0;
+                        if constexpr (ND % 4 == 0) {
+#pragma unroll
+                            for (int e = 0; e < ND; e += 4) {
+                                const float4 t = *reinterpret_cast<const float4*>(xs + e);
+                                x[u][j][e] = t.x;
+                                x[u][j][e + 1] = t.y;
+                                x[u][j][e + 2] = t.z;
+                                x[u][j][e + 3] = t.w;
+                            }
+                        } else if constexpr (ND == 2) {
+                            const float2 t = *reinterpret_cast<const float2*>(xs);
+                            x[u][j][0] = t.x;
+                            x[u][j][1] = t.y;
+                        } else {
+                            x[u][j][0] = xs[0];
+                        }
+                    }
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    if (i0 + u >= nb) continue;
+                    if (cb + i0 + u == 0) {
+                        Lr[j] = f[u][j].z;
+#pragma unroll
+                        for (int e = 0; e < ND; ++e) A[j][e] = x[u][j][e];
+                    } else {
+                        const float fo = f[u][j].x, fc = f[u][j].y;
+                        Lr[j] = bi_attn::fold_value(Lr[j], fo, f[u][j].z, fc);
+#pragma unroll
+                        for (int e = 0; e < ND; ++e) A[j][e] = bi_attn::fold_value(A[j][e], fo, x[u][j][e], fc);
+                    }
+                }
+        }
+        __syncthreads();  // staging is reused by the next batch
+    }
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+        __nv_bfloat16* o = a.out + (row0 + h0 + j) * kD + d0;
+        if constexpr (ND % 2 == 0) {
+#pragma unroll
+            for (int e = 0; e < ND; e += 2)
+                *reinterpret_cast<__nv_bfloat162*>(o + e) = __halves2bfloat162(
+                    __float2bfloat16_rn(__fdiv_rn(A[j][e], Lr[j])),
+                    __float2bfloat16_rn(__fdiv_rn(A[j][e + 1], Lr[j])));
+        } else {
+            o[0] = __float2bfloat16_rn(__fdiv_rn(A[j][0], Lr[j]));
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -118,6 +279,10 @@ __global__ void __launch_bounds__(kThreads)
     if (c0 >= nch) return;
     const int c1 = min(nch, c0 + a.chunks_per_cta);
     const bool whole = (c0 == 0 && c1 == nch);  // this CTA folds the whole sequence
+    // several CTAs share the sequence and the last one to arrive folds it
+    const bool shared_fold = !whole && a.counters != nullptr;
+    const uint32_t ngroups = static_cast<uint32_t>((nch + a.chunks_per_cta - 1) / a.chunks_per_cta);
+    uint32_t* const ctr = shared_fold ? a.counters + static_cast<int64_t>(s) * a.Hkv + g : nullptr;
     const int npg_total = (L + kPage - 1) / kPage;
     const int pg0 = c0 * ppc;
     const int npg_group = min(c1 * ppc, npg_total) - pg0;
@@ -150,7 +315,15 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
     if (bad_page) {
-        if (tid == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+        if (tid == 0) {
+            bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+            if (shared_fold) {
+                // count in, marking the sequence bad (its output stays
+                // unwritten); the last arrival still returns the counter to 0
+                const uint32_t now = bi::atomic_add_acq_rel_gpu(ctr, kArriveBad) + kArriveBad;
+                if ((now & 0xffffu) == ngroups) atomicExch(ctr, 0u);
+            }
+        }
         return;
     }
 
@@ -192,7 +365,8 @@ __global__ void __launch_bounds__(kThreads)
     }
     const int h0 = 2 * (lane & 3);
     bool timed_out = false;
-    int j = 0;  // this warp's page counter (matches the loader's)
+    int j = 0;       // this warp's page counter (matches the loader's)
+    int j_fail = 0;  // first page whose wait timed out
     const int rounds = (c1 - c0 + kWarps - 1) / kWarps;
 
     for (int r = 0; r < rounds; ++r) {
@@ -206,6 +380,7 @@ __global__ void __launch_bounds__(kThreads)
                 if (timed_out) continue;
                 if (!bi::mbar_wait(&bars[stg], (j / kSPW) & 1)) {
                     timed_out = true;
+                    j_fail = j;
                     continue;
                 }
                 const int valid = min(kPage, L - (c * ppc + p) * kPage);
@@ -292,13 +467,48 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
 
-    if (timed_out && lane == 0) bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+    if (timed_out && lane == 0) {
+        bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+        // pages j_fail .. lj-1 were issued and never seen to land (at most kSPW):
+        // give each one more bounded wait before this warp's stages are released
+        for (int i = j_fail; i < lj; ++i)
+            bi::mbar_wait_for(&bars[warp * kSPW + i % kSPW], (i / kSPW) & 1, bi::kDrainNs);
+    }
     if (whole) {
         const int d = tid;
         for (int h = 0; h < a.group; ++h) {
             const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
             a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(fold_o[h * kD + d], fold_l[h]));
         }
+        return;
+    }
+    if (!shared_fold) return;  // the merge kernel folds
+
+    // ---- arrival: the last CTA of this (sequence, kv-head) folds it ------
+    __shared__ int fold_here;
+    __syncthreads();  // every warp's partial stores precede the arrival
+    if (tid == 0) {
+        // release: this CTA's partials are visible before its arrival counts;
+        // acquire: the last arrival sees every other CTA's partials
+        const uint32_t now = bi::atomic_add_acq_rel_gpu(ctr, kArrive) + kArrive;
+        const bool last = (now & 0xffffu) == ngroups;
+        if (last) {
+            atomicExch(ctr, 0u);  // ready for the next call
+            if (now >> 16) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+        }
+        fold_here = last && (now >> 16) == 0;
+    }
+    __syncthreads();
+    if (!fold_here) return;
+    switch (a.group) {
+        case 1: fold_sequence<1>(a, s, g, nch, smem, fold_o, tid); break;
+        case 2: fold_sequence<2>(a, s, g, nch, smem, fold_o, tid); break;
+        case 3: fold_sequence<3>(a, s, g, nch, smem, fold_o, tid); break;
+        case 4: fold_sequence<4>(a, s, g, nch, smem, fold_o, tid); break;
+        case 5: fold_sequence<5>(a, s, g, nch, smem, fold_o, tid); break;
+        case 6: fold_sequence<6>(a, s, g, nch, smem, fold_o, tid); break;
+        case 7: fold_sequence<7>(a, s, g, nch, smem, fold_o, tid); break;
+        default: fold_sequence<8>(a, s, g, nch, smem, fold_o, tid); break;
     }
 }
 
@@ -367,7 +577,8 @@ extern "C" size_t bi_decode_attention_workspace_size(int32_t B, int32_t Hq, int3
     if (B < 0 || Hq <= 0 || D <= 0 || max_seq_len < 1) return 0;
     const int64_t chunks = ceil_div(max_seq_len, kChunk);
     if (chunks < 2) return 0;
-    return static_cast<size_t>(B) * Hq * chunks * (static_cast<size_t>(D) + 2) * sizeof(float);
+    return BI_DECODE_COUNTER_BYTES +
+           static_cast<size_t>(B) * Hq * chunks * (static_cast<size_t>(D) + 2) * sizeof(float);
 }
 
 extern "C" int32_t bi_decode_num_chunks(int32_t seq_len) {
@@ -382,14 +593,22 @@ extern "C" int32_t bi_decode_chunk_len(int32_t seq_len, int32_t c) {
 
 namespace {
 
-// Schedule (never the arithmetic): how many consecutive chunks one CTA
-// walks -- enough CTAs for about four waves of the resident slots (3 CTAs per
-// SM), between 4 (one per warp) and 32.
+// Schedule (never the arithmetic): how many consecutive chunks one CTA walks.
+// Measured on GB300 (cold L2, lengths uniform up to the bound, 3 CTAs per SM):
+//   - 4 (one chunk per warp) is fastest from one sequence up to 2^16
+//     (sequence, kv-head, chunk) units in the launch: B = 1 .. 128 at 8192
+//     tokens (B = 128: 313 us against 318-336 us for 6 .. 32);
+//   - from 2^16 units on, 32: the CTA holds whole sequences and folds them
+//     without partials (B = 256: 599 against 605 us);
+//   - when groups of 4 would fill between one and two waves of the resident
+//     slots (about half the bound's CTAs have work when lengths spread up to
+//     the bound), groups of 8 fit in one wave: B = 16, 57 against 62 us.
 int chunks_per_cta(int64_t B, int64_t Hkv, int64_t max_chunks, int sms) {
     const int64_t slots = static_cast<int64_t>(sms) * 3;
-    const int64_t units = B * Hkv * max_chunks;
-    return static_cast<int>(
-        std::min<int64_t>(kMaxChunksPerCta, std::max<int64_t>(kWarps, units / (4 * slots))));
+    if (B * Hkv * max_chunks >= (int64_t{1} << 16)) return kMaxChunksPerCta;
+    const int64_t ctas4 = B * Hkv * ((max_chunks + kWarps - 1) / kWarps);
+    if (ctas4 > 2 * slots && ctas4 <= 4 * slots) return 2 * kWarps;
+    return kWarps;
 }
 
 // Validate and launch split + merge.  num_splits == 0 is the batch-invariant
@@ -421,8 +640,9 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
         (reinterpret_cast<uintptr_t>(seq_lens) & 3))
         return BI_ERR_MISALIGNED;
     const int max_chunks = num_splits > 0 ? num_splits : ceil_div(max_seq_len, kChunk);
-    const size_t need = max_chunks >= 2 ? static_cast<size_t>(B) * Hq * max_chunks *
-                                              (static_cast<size_t>(D) + 2) * sizeof(float)
+    const size_t need = max_chunks >= 2 ? BI_DECODE_COUNTER_BYTES +
+                                              static_cast<size_t>(B) * Hq * max_chunks *
+                                                  (static_cast<size_t>(D) + 2) * sizeof(float)
                                         : 0;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return BI_ERR_WORKSPACE_TOO_SMALL;
@@ -449,10 +669,12 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     args.block_table = block_table;
     args.seq_lens = seq_lens;
     args.out = static_cast<__nv_bfloat16*>(out);
-    args.ws_acc = need ? static_cast<float*>(workspace) : nullptr;
-    args.ws_ml = need ? static_cast<float*>(workspace) +
-                            static_cast<size_t>(B) * Hq * max_chunks * kD
-                      : nullptr;
+    // workspace: [counters, BI_DECODE_COUNTER_BYTES][acc partials][(m, l) partials]
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const bool counted = need && static_cast<int64_t>(B) * Hkv <= kMaxCounters;
+    args.counters = counted ? reinterpret_cast<uint32_t*>(ws) : nullptr;
+    args.ws_acc = need ? reinterpret_cast<float*>(ws + BI_DECODE_COUNTER_BYTES) : nullptr;
+    args.ws_ml = need ? args.ws_acc + static_cast<size_t>(B) * Hq * max_chunks * kD : nullptr;
     args.err = bi::device_error_word();
     args.max_pages_per_seq = max_pages_per_seq;
     args.Hq = Hq;
@@ -465,7 +687,9 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
     // A sequence whose chunks all fall to one CTA is folded there, the rest by
-    // the merge kernel -- both apply the same fold in the same chunk order.
+    // the last of its CTAs to arrive (or by the merge kernel when there are
+    // more (sequence, kv-head) pairs than counters) -- every one of them
+    // applies the same fold in the same chunk order.
     int cpc = 1;
     if (num_splits == 0) {
         cpc = chunks_per_cta(B, Hkv, max_chunks, bi::sm_count());
@@ -479,7 +703,7 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     if (bi::launch_pdl(attn_split_kernel, dim3(groups, Hkv, B), dim3(kThreads), kSmemBytes, stream,
                        tk, tv, args) != cudaSuccess)
         return BI_ERR_CUDA;
-    if (max_chunks > cpc) {
+    if (max_chunks > cpc && !counted) {
         // few rows: each thread's chain of loads is the bound, so load up to
         // 32 chunks at once; many rows: 8, for more resident CTAs
         const cudaError_t e =
@@ -504,7 +728,8 @@ extern "C" int32_t bi_decode_attention_launches(int32_t B, int32_t Hkv, int32_t 
     const int sms = bi::sm_count();
     if (sms <= 0) return 0;
     const int max_chunks = ceil_div(max_seq_len, kChunk);
-    return max_chunks > chunks_per_cta(B, Hkv, max_chunks, sms) ? 2 : 1;
+    const bool counted = static_cast<int64_t>(B) * Hkv <= kMaxCounters;
+    return max_chunks > chunks_per_cta(B, Hkv, max_chunks, sms) && !counted ? 2 : 1;
 }
 
 extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache,
@@ -538,11 +763,14 @@ extern "C" bi_status bi_decode_attention_fixed_splits(
 namespace {
 
 // Capacity in chunk partials (one per sequence x query head x 256-token
-// chunk), each kD + 2 floats: 65536 x 130 x 4 bytes = 32.5 MiB per device.
+// chunk), each kD + 2 floats: 65536 x 130 x 4 bytes = 32.5 MiB per device,
+// after the arrival counters (zero when the library is loaded, and every call
+// leaves them zero).
 constexpr int64_t kNoAllocPartials = 65536;
-constexpr size_t kNoAllocBytes = static_cast<size_t>(kNoAllocPartials) * (kD + 2) * sizeof(float);
+constexpr size_t kNoAllocBytes =
+    BI_DECODE_COUNTER_BYTES + static_cast<size_t>(kNoAllocPartials) * (kD + 2) * sizeof(float);
 
-static __device__ __align__(256) float g_noalloc_scratch[kNoAllocPartials * (kD + 2)];
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocBytes / sizeof(float)];
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64] = {};
@@ -550,10 +778,14 @@ void* g_noalloc_ptr[64] = {};
 // Device address of g_noalloc_scratch on the current device.  The host-side
 // name of the array is only a stand-in; the address a kernel can use comes
 // from cudaGetSymbolAddress, resolved once per device with that device
-// current and cached.
-void* noalloc_scratch_address(int dev) {
+// current and cached.  The first call on a device must not come while the
+// stream is being captured (the lookup may load the module): refused then.
+void* noalloc_scratch_address(int dev, cudaStream_t stream) {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+            return nullptr;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
         g_noalloc_ptr[dev] = p;
@@ -571,14 +803,17 @@ extern "C" bi_status bi_decode_attention_noalloc(const void* q, const void* k_ca
                                                  int32_t num_pages, int32_t max_seq_len,
                                                  float scale, void* out, cudaStream_t stream) {
     if (B < 0 || Hq <= 0 || max_seq_len < 1) return BI_ERR_INVALID_ARG;
-    const int64_t partials = static_cast<int64_t>(B) * Hq * ceil_div(max_seq_len, kChunk);
+    // a call whose sequences all fit in one chunk writes no partials at all
     const size_t need = bi_decode_attention_workspace_size(B, Hq, D, max_seq_len);
-    if (need > kNoAllocBytes || partials > kNoAllocPartials) return BI_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0) {
+        const int64_t partials = static_cast<int64_t>(B) * Hq * ceil_div(max_seq_len, kChunk);
+        if (need > kNoAllocBytes || partials > kNoAllocPartials) return BI_ERR_WORKSPACE_TOO_SMALL;
+    }
     void* ws = nullptr;
     if (need > 0) {
         int dev = -1;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
-        ws = noalloc_scratch_address(dev);
+        ws = noalloc_scratch_address(dev, stream);
         if (!ws) return BI_ERR_CUDA;
     }
     return bi_decode_attention(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, B,

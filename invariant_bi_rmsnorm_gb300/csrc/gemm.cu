@@ -72,7 +72,7 @@ constexpr int BNC = BN / 2;  // W rows per CTA
 constexpr int BK = 64;
 constexpr int kStages = 7;
 constexpr int kABytes = BMC * BK * 2;  // 16 KiB
-constexpr int kBBytes = BNC * BK * 2;  // 14 KiB
+constexpr int kBBytes = BNC * BK * 2;  // 16 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
@@ -109,7 +109,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     uint64_t* empty = full + kStages;
     uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* drain = tempty + 2;  // MMA completion after a timeout
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int s_timeout;    // a role of this CTA gave up on a wait
+    __shared__ int s_issued;     // k-block loads the producer issued
+    __shared__ int s_consumed;   // k-block loads the MMA thread saw land
 
     const uint32_t rank = bi::cluster_ctarank();
     const bool leader = rank == 0;
@@ -131,7 +135,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             bi::mbar_init(&tfull[i], 1);
             bi::mbar_init(&tempty[i], 8);  // 4 epilogue warps in each CTA (leader's copy used)
         }
+        bi::mbar_init(drain, 1);
         bi::fence_mbar_init();
+        s_timeout = 0;
+        s_issued = 0;
+        s_consumed = 0;
         bi::tma_prefetch_desc(&tmap_x);
         bi::tma_prefetch_desc(&tmap_w);
     }
@@ -152,12 +160,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int issued = 0;
             for (int tile = pair_id; tile < num_tiles; tile += npairs) {
                 int mb, nb;
                 tile_coords(tile, num_m, num_n, group_m, mb, nb);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!bi::mbar_wait(&empty[stage], phase ^ 1)) {
                         bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmProducer);
+                        s_timeout = 1;
                         goto producer_done;
                     }
                     uint8_t* sa = smem + stage * kStageBytes;
@@ -167,13 +177,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                                          mb * BMP + static_cast<int>(rank) * BMC);
                     bi::tma_load_2d_pair(sa + kABytes, &tmap_w, full_leader, kb * BK,
                                          nb * BN + static_cast<int>(rank) * BNC);
+                    ++issued;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-        producer_done:;
+        producer_done:
+            s_issued = issued;
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
@@ -181,9 +193,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            int consumed = 0;
+            bool issued_any = false;
             for (int tile = pair_id; tile < num_tiles; tile += npairs) {
                 if (!bi::mbar_wait(&tempty[acc], acc_phase ^ 1)) {
                     bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmMma);
+                    s_timeout = 1;
                     break;
                 }
                 bi::tc_fence_after();
@@ -192,9 +207,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!bi::mbar_wait(&full[stage], phase)) {
                         bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmMma);
+                        s_timeout = 1;
                         ok = false;
                         break;
                     }
+                    ++consumed;
+                    issued_any = true;
                     bi::tc_fence_after();
                     const uint32_t sa = bi::smem_u32(smem + stage * kStageBytes);
                     const uint32_t sb = sa + kABytes;
@@ -217,6 +235,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                     acc_phase ^= 1;
                 }
             }
+            s_consumed = consumed;
+            if (s_timeout && issued_any) {
+                // the MMAs issued so far may still be reading shared memory and
+                // writing TMEM: a bounded wait for them before both are freed
+                bi::tc_commit_pair_multicast(drain, 0x1);
+                bi::mbar_wait_for(drain, 0, bi::kDrainNs);
+            }
         }
     } else {
         // epilogue warps 2..5 -> TMEM lane quarter warp % 4 of this CTA's 128 rows
@@ -227,7 +252,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             int mb, nb;
             tile_coords(tile, num_m, num_n, group_m, mb, nb);
             if (!bi::mbar_wait(&tfull[acc], acc_phase)) {
-                if (lane == 0) bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmEpilogue);
+                if (lane == 0) {
+                    bi::report_error(err, bi::kErrTimeout | bi::kWhereGemmEpilogue);
+                    s_timeout = 1;
+                }
                 break;
             }
             bi::tc_fence_after();
@@ -282,6 +310,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
     }
 
+    __syncthreads();
+    if (s_timeout && leader && threadIdx.x == 0) {
+        // Loads issued but never seen to land (at most one ring's worth): a
+        // bounded wait for each before the pair's shared memory is released.
+        // The leader's barriers count both CTAs' bytes, and both producers
+        // walk the same stage sequence, so this covers the peer's copies.
+        for (int i = s_consumed; i < s_issued; ++i)
+            bi::mbar_wait_for(&full[i % kStages], (i / kStages) & 1, bi::kDrainNs);
+    }
     bi::tc_fence_before();
     bi::cluster_sync();  // both CTAs past their last TMEM access and remote arrive
     if (warp == 1) {

@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kConsumerWarps) {
         // ---------------- producer: every page the tile needs, in order ----
         if (lane == 0) {
-            for (int k = 0; k < npg; ++k) {
+            int k = 0;
+            for (; k < npg; ++k) {
                 const int st = k % kStages;
                 if (!bi::mbar_wait(&empty[st], ((k / kStages) & 1) ^ 1)) {
                     bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
@@ -143,6 +144,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 bi::tma_load_3d(kd, &tmap_k, &full[st], 0, row, 0);
                 bi::tma_load_3d(vd, &tmap_v, &full[st], 0, row, 0);
             }
+            // the CTA's shared memory outlives no copy: wait (bounded) for the
+            // last copy issued into each stage -- on a healthy run the
+            // consumers wait for the same copies
+            for (int i = max(0, k - kStages); i < k; ++i)
+                bi::mbar_wait_for(&full[i % kStages], (i / kStages) & 1, bi::kDrainNs);
         }
         return;
     }
@@ -202,7 +208,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             bi::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) bi::mbar_arrive(&empty[stg]);
+            // a warp that timed out stops handing stages back, so the producer
+            // stops too (its own wait on the stage runs out) and drains
+            if (lane == 0 && !timed_out) bi::mbar_arrive(&empty[stg]);
         }
         // fold chunk c into each column whose row sees it, as the decode path does
 #pragma unroll

@@ -26,9 +26,23 @@ import torch
 
 from . import (add_rmsnorm, decode_attention, decode_attention_workspace_size, gemm,
                gemm_swiglu, interleave_gate_up, logprobs, prefill_attention,
-               qk_norm_rope_append, rmsnorm, rope_table, silu_mul)
+               qk_norm_rope_append, rmsnorm, silu_mul)
 from . import inputs
 from ._lib import PAGE_SIZE
+
+
+def rope_table(max_pos: int, theta: float, D: int = 128, device=None) -> torch.Tensor:
+    """The model's RoPE table, an input of bi_qk_norm_rope_append like a
+    weight: fp32 [max_pos][D] with cos(pos * f_i) at i and sin(pos * f_i) at
+    D/2 + i, f_i = theta^(-i/(D/2)) (rotate-half pairing), evaluated in float64
+    on the host and rounded once to fp32."""
+    half = D // 2
+    pos = torch.arange(max_pos, dtype=torch.float64)[:, None]
+    f = torch.pow(torch.tensor(float(theta), dtype=torch.float64),
+                  -torch.arange(half, dtype=torch.float64) / half)[None, :]
+    ang = pos * f
+    tab = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+    return tab.to(device) if device is not None else tab
 
 
 @dataclass
@@ -136,6 +150,7 @@ class Engine:
         self.pad_page = num_pages - 1 if cuda_graphs else None
         self.free_pages = deque(range(num_pages - 1 if cuda_graphs else num_pages))
         self._graphs = {}
+        self._ws = None
         self.graph_steps = 0
         self.rope = rope_table(cfg.max_pos, cfg.rope_theta, D, device=self.device)
         T, H, F = max_tokens_per_step, cfg.hidden, cfg.ffn
@@ -225,6 +240,7 @@ class Engine:
             lens = [s.n_cached + 1 for _, s, _ in dec]
             bt = table(dec)
             meta["dec"] = (self._rows(rows, up), i32(bt), i32(lens), int(max(lens)), bt.shape[1])
+            meta["ws"] = self._att_workspace(len(dec), int(max(lens)))
         if pre:
             starts = [int(offs[k]) for k, _, _ in pre]
             nqs = [n for _, _, n in pre]
@@ -289,7 +305,8 @@ class Engine:
               "lens": torch.ones(Bb, **i32),
               "bt": torch.full((Bb, W), self.pad_page, **i32),
               "logits": torch.empty(Bb, cfg.vocab, dtype=torch.bfloat16, device=dev),
-              "ws": torch.empty(decode_attention_workspace_size(Bb, cfg.heads, cfg.head_dim,
+              # zero-filled: its leading arrival counters must start at zero
+              "ws": torch.zeros(decode_attention_workspace_size(Bb, cfg.heads, cfg.head_dim,
                                                                 cfg.max_pos),
                                 dtype=torch.uint8, device=dev)}
         meta = {"dec": (slice(0, Bb), st["bt"], st["lens"], cfg.max_pos, W), "ws": st["ws"]}
@@ -351,6 +368,20 @@ class Engine:
         self.steps += 1
         self.graph_steps += 1
         return st["logits"][:B]
+
+    def _att_workspace(self, B: int, max_len: int):
+        """The eager steps' decode-attention workspace, kept across steps and
+        grown when a step needs more.  It is zero-filled when allocated: its
+        leading arrival counters must start at zero, and every call leaves
+        them zero, so it is never cleared again."""
+        cfg = self.cfg
+        need = decode_attention_workspace_size(B, cfg.heads, cfg.head_dim, max_len)
+        if need == 0:
+            return None
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = None
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self._ws
 
     def _ops(self):
         if self.ops == "bi":

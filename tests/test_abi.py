@@ -34,7 +34,7 @@ def test_library_exports_every_declared_entry_point(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.bi_abi_version() == 1
+    assert lib.bi_abi_version() == 2
     for code, name in [(0, "BI_OK"), (1, "BI_ERR_INVALID_ARG"), (2, "BI_ERR_UNSUPPORTED_SHAPE"),
                        (3, "BI_ERR_MISALIGNED"), (4, "BI_ERR_WORKSPACE_TOO_SMALL"),
                        (5, "BI_ERR_CUDA"), (6, "BI_ERR_DEVICE_TIMEOUT"),
@@ -74,9 +74,11 @@ def test_chunk_plan_properties(lib, L):
 
 
 def test_workspace_size(lib):
-    assert lib.bi_decode_attention_workspace_size(256, 32, 128, 8192) == 256 * 32 * 32 * 130 * 4
+    ctr = _lib.DECODE_COUNTER_BYTES  # arrival counters ahead of the partials
+    assert ctr == 262144
+    assert lib.bi_decode_attention_workspace_size(256, 32, 128, 8192) == ctr + 256 * 32 * 32 * 130 * 4
     assert lib.bi_decode_attention_workspace_size(4, 32, 128, 256) == 0  # single chunk
-    assert lib.bi_decode_attention_workspace_size(4, 32, 128, 257) == 4 * 32 * 2 * 130 * 4
+    assert lib.bi_decode_attention_workspace_size(4, 32, 128, 257) == ctr + 4 * 32 * 2 * 130 * 4
     assert lib.bi_decode_attention_workspace_size(-1, 32, 128, 1000) == 0
 
 
@@ -153,3 +155,13 @@ def test_binding_refuses_cpu_tensors():
         bi.rmsnorm(x, torch.ones(64, dtype=torch.bfloat16))
     with pytest.raises(ValueError, match="CUDA"):
         bi.gemm(x, x)
+
+
+def test_noalloc_size_limit_is_checked_on_the_host(lib):
+    f = lib.bi_decode_attention_noalloc
+    # (q, k, v, bt, max_pages, lens, B, Hq, Hkv, D, page, num_pages, max_seq_len, scale, out, stream)
+    # 2 x 32 x 1025 chunk partials > 65536: refused before any device work
+    assert f(FAKE, FAKE, FAKE, FAKE, 16400, FAKE, 2, 32, 8, 128, 16, 256, 1025 * 256, 0.088,
+             FAKE, None) == _lib.BI_ERR_WORKSPACE_TOO_SMALL
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, FAKE, -1, 32, 8, 128, 16, 256, 1000, 0.088,
+             FAKE, None) == _lib.BI_ERR_INVALID_ARG

@@ -68,11 +68,35 @@ def test_edge_lengths_against_oracle():
     _check(_run(p), oracle.decode_attention(**p))
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4), (32, 8), (64, 8), (24, 8)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (24, 8), (16, 4), (32, 8), (40, 8),
+                                    (48, 8), (56, 8), (64, 8)])
 def test_gqa_group_sizes(Hq, Hkv):
-    lens = [3, 300, 1000]
-    p = inputs.decode_problem(3, Hq=Hq, Hkv=Hkv, seq_lens=lens, seed=210 + Hq)
+    # group sizes 1 .. 8; the 3000- and 9000-token sequences span several
+    # CTAs, so the last-arriving CTA folds them (9000 tokens: 36 chunks, more
+    # than one scan block or staging batch for every group size)
+    lens = [3, 300, 1000, 3000, 9000]
+    p = inputs.decode_problem(len(lens), Hq=Hq, Hkv=Hkv, seq_lens=lens, seed=210 + Hq)
     _check(_run(p), oracle.decode_attention(**p))
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 8])
+def test_last_cta_fold_equals_in_cta_fold_for_every_group_size(G):
+    # In a batch of 256 each sequence (up to 32 chunks) is walked and folded
+    # by one CTA; alone it is spread over up to 8 CTAs and folded by the last
+    # to arrive.  Same operations in the same order: same bits.
+    B, Hkv = 256, 8
+    p = inputs.decode_problem(B, Hq=G * Hkv, Hkv=Hkv, max_len=8192, seed=400 + G, device="cuda")
+    lib = bi._lib.load()
+    full = bits(_run(p, max_seq_len=8192))
+    lens = p["seq_lens"]
+    pick = [int(i) for i in torch.argsort(lens, descending=True)[:3]] + [int(torch.argmin(lens))]
+    for s in pick:
+        one = {k: (v[s:s + 1] if k in ("q", "block_table", "seq_lens") else v) for k, v in p.items()}
+        assert np.array_equal(bits(_run(one, max_seq_len=8192))[0], full[s]), f"sequence {s}"
+    assert lib.bi_decode_attention_launches(1, Hkv, 8192) == 1
+    sub = _host_subset(p, np.array(pick))
+    rows = torch.from_numpy(full[pick].view(np.int16)).view(torch.bfloat16)
+    _check(rows, oracle.decode_attention(**sub))
 
 
 def test_custom_scale():
@@ -195,7 +219,7 @@ def test_complete_chunk_partials_stable_as_cache_grows():
         p["seq_lens"] = torch.tensor([L], dtype=torch.int32)
         ws.zero_()
         _run(p, max_seq_len=2048, workspace=ws)
-        f = ws.view(torch.float32)
+        f = ws[bi.DECODE_COUNTER_BYTES:].view(torch.float32)  # after the arrival counters
         return (f[:acc_elems].view(Hq, max_chunks, D).cpu().numpy().copy(),
                 f[acc_elems:].view(Hq, max_chunks, 2).cpu().numpy().copy())
 
@@ -236,6 +260,76 @@ def test_c4_full_size_sampled_parity():
         _check(out[torch.from_numpy(pick).cuda()], oracle.decode_attention(**sub))
 
 
+def test_one_launch_folds_in_the_last_cta_and_leaves_counters_zero():
+    # A sequence spread over several CTAs is folded by the last of them to
+    # arrive, in the same launch: one kernel for every C4 batch.  The
+    # workspace's arrival counters are back at zero after each call, so the
+    # same workspace serves the next call (same bits), and the result matches
+    # the oracle.
+    lib = bi._lib.load()
+    for B in (1, 16, 128, 256):
+        assert lib.bi_decode_attention_launches(B, 8, 8192) == 1
+    B = 16
+    p = inputs.decode_problem(B, max_len=8192, seed=330)
+    d = _to_dev(p)
+    ws = torch.zeros(bi.decode_attention_workspace_size(B, 32, 128, 8192), dtype=torch.uint8,
+                     device="cuda")
+    counters = ws[:bi.DECODE_COUNTER_BYTES].view(torch.int32)
+    outs = []
+    for _ in range(3):
+        outs.append(bits(bi.decode_attention(d["q"], d["k_cache"], d["v_cache"],
+                                             d["block_table"], d["seq_lens"], max_seq_len=8192,
+                                             workspace=ws)))
+        assert int(counters.count_nonzero()) == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    # the long sequences really were spread over several CTAs (partials written)
+    assert int(ws[bi.DECODE_COUNTER_BYTES:].count_nonzero()) > 0
+    pick = np.arange(0, B, 3)
+    out = torch.from_numpy(outs[0][pick].view(np.int16)).view(torch.bfloat16)
+    _check(out, oracle.decode_attention(**_host_subset(p, pick)))
+    # a sequence alone (more CTAs per sequence) gives the batched bits
+    for s in (0, 7):
+        sl = slice(s, s + 1)
+        alone = bits(bi.decode_attention(d["q"][sl], d["k_cache"], d["v_cache"],
+                                         d["block_table"][sl], d["seq_lens"][sl],
+                                         max_seq_len=8192, workspace=ws))
+        assert np.array_equal(alone[0], outs[0][s])
+        assert int(counters.count_nonzero()) == 0
+
+
+def test_more_sequence_heads_than_counters_fall_back_to_the_merge_kernel():
+    # 2049 sequences x 32 kv-heads is more (sequence, kv-head) pairs than the
+    # workspace has arrival counters: sequences spread over several CTAs are
+    # then folded by the separate merge kernel, with the same fold -- the bits
+    # equal those of the same sequences run alone (one launch, counters).
+    lib = bi._lib.load()
+    B, Hq, Hkv, msl = 2049, 32, 32, 8448  # 33 chunks: more than one CTA walks
+    assert B * Hkv > bi.DECODE_COUNTER_BYTES // 4
+    assert lib.bi_decode_attention_launches(B, Hkv, msl) == 2
+    assert lib.bi_decode_attention_launches(1, Hkv, msl) == 1
+    special = {0: 8448, 1000: 5000, 2048: 300}
+    base = inputs.decode_problem(3, Hq=Hq, Hkv=Hkv, seq_lens=list(special.values()), seed=340)
+    width = msl // 16
+    bt = torch.zeros(B, width, dtype=torch.int32)
+    lens = torch.ones(B, dtype=torch.int32)
+    bt[:] = base["block_table"][2, 0]  # length-1 rows read one page of the short sequence
+    for j, (s, L) in enumerate(special.items()):
+        n = -(-L // 16)
+        bt[s, :n] = base["block_table"][j, :n]
+        lens[s] = L
+    q = inputs.decode_queries(B, Hq, 128, seed=341)
+    kc, vc = base["k_cache"].cuda(), base["v_cache"].cuda()
+    qd, btd, ld = q.cuda(), bt.cuda(), lens.cuda()
+    big = bits(bi.decode_attention(qd, kc, vc, btd, ld, max_seq_len=msl))
+    for j, s in enumerate(special):
+        sl = slice(s, s + 1)
+        alone = bi.decode_attention(qd[sl], kc, vc, btd[sl], ld[sl], max_seq_len=msl)
+        assert np.array_equal(bits(alone)[0], big[s]), f"sequence {s}"
+        one = {"q": q[sl], "k_cache": base["k_cache"], "v_cache": base["v_cache"],
+               "block_table": bt[sl], "seq_lens": lens[sl]}
+        _check(alone, oracle.decode_attention(**one))
+
+
 def test_device_side_bad_inputs_reported_without_fault():
     p = inputs.decode_problem(3, seq_lens=[10, 20, 30], seed=280)
     d = _to_dev(p)
@@ -249,6 +343,22 @@ def test_device_side_bad_inputs_reported_without_fault():
     bi.decode_attention(d["q"], d["k_cache"], d["v_cache"], bad_bt, d["seq_lens"], max_seq_len=30)
     with pytest.raises(bi.BiError, match="BAD_INPUT"):
         bi.get_device_error()
+    # a bad page in one CTA of a sequence spread over several CTAs: reported,
+    # and the arrival counter still goes back to zero for the next call
+    q = inputs.decode_problem(2, seq_lens=[3000, 2000], seed=281)
+    dq = _to_dev(q)
+    ws = torch.zeros(bi.decode_attention_workspace_size(2, 32, 128, 3000), dtype=torch.uint8,
+                     device="cuda")
+    bad_bt = dq["block_table"].clone()
+    bad_bt[0, 100] = -5  # a page in chunk 6 (CTA 1 of 3)
+    bi.decode_attention(dq["q"], dq["k_cache"], dq["v_cache"], bad_bt, dq["seq_lens"],
+                        max_seq_len=3000, workspace=ws)
+    with pytest.raises(bi.BiError, match="BAD_INPUT"):
+        bi.get_device_error()
+    assert int(ws[:bi.DECODE_COUNTER_BYTES].count_nonzero()) == 0
+    good = bi.decode_attention(dq["q"], dq["k_cache"], dq["v_cache"], dq["block_table"],
+                               dq["seq_lens"], max_seq_len=3000, workspace=ws)
+    _check(good, oracle.decode_attention(**q))
     # the context is still usable and later calls are clean
     _check(_run(p), oracle.decode_attention(**p))
     bi.get_device_error()

@@ -17,7 +17,7 @@ import torch
 
 import invariant_bi_rmsnorm_gb300 as bi
 import oracle
-from invariant_bi_rmsnorm_gb300 import inputs
+from invariant_bi_rmsnorm_gb300 import inputs, qwen3
 from oracle import decoder as odec
 from tests._util import bits, f64, ulp_distance
 
@@ -61,7 +61,7 @@ def test_qk_norm_rope_append_against_oracle():
     slots = perm.to(torch.int32)
     kc = torch.zeros(num_pages, Hkv, 16, D, dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
-    rope = bi.rope_table(4096, 1e6, D, device="cuda")
+    rope = qwen3.rope_table(4096, 1e6, D, device="cuda")
     q = bi.qk_norm_rope_append(qkv.cuda(), Hq, Hkv, pos.cuda(), slots.cuda(), rope, qn.cuda(),
                                kn.cuda(), kc, vc, 1e-6)
     x = qkv.double().numpy().reshape(T, Hq + 2 * Hkv, D)
