@@ -382,8 +382,7 @@ class Workload:
             if unit == "TFLOP/s":
                 entry["frac_of_measured_bf16_burst"] = round(rate / bf16, 4)
                 entry["gbs"] = round(info.pop("bytes") / t / 1e6, 1)
-                entry["bound"] = ("tensor (tcgen05)" if name == "gemm_swiglu"
-                                  else "tensor (mma.sync m16n8k16, not tcgen05)")
+                entry["bound"] = "tensor (tcgen05)"
             else:
                 entry["frac_of_measured_hbm"] = round(rate / hbm, 4)
                 entry["bound"] = "hbm"
@@ -877,9 +876,11 @@ def build_next_case(name: str, dev, bi, inputs):
         a = {k: v.to(dev) for k, v in p.items() if k != "q"}
         indptr = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
         out = torch.empty(tot, HQ, HD, dtype=torch.bfloat16, device=dev)
+        pws = torch.empty(max(1, bi.prefill_attention_workspace_size(tot, HQ, HD, max(lens))),
+                          dtype=torch.uint8, device=dev)
         fn = lambda: bi.prefill_attention(q, a["k_cache"], a["v_cache"], a["block_table"],  # noqa: E731
                                           a["seq_lens"], indptr, max_q_len=max(lens),
-                                          max_seq_len=max(lens), out=out)
+                                          max_seq_len=max(lens), out=out, workspace=pws)
         flops = float(sum(4.0 * HD * HQ * L * (L + 1) / 2 for L in lens))
         nbytes = float(2 * tot * HQ * HD * 2 + sum(L * HKV * HD * 4 for L in lens))
         return fn, flops, "TFLOP/s", {"sequences": len(lens), "tokens": tot,

@@ -268,7 +268,12 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
  *                its query rows (n_i <= seq_lens[i] <= max_seq_len).
  *   block_table  device, int32 [S][max_pages_per_seq], as bi_decode_attention.
  *   max_q_len    host bound on every n_i (sizes the grid).
- *   S <= 65535; other arguments as bi_decode_attention.  No workspace.
+ *   workspace    device, >= bi_prefill_attention_workspace_size(T, Hq, D,
+ *                max_seq_len) bytes, 16-byte aligned; may be null when that
+ *                size is 0 (no row longer than 256 tokens).  It holds the fp32
+ *                running output of rows longer than one chunk between chunks;
+ *                its contents need no initialisation and are undefined after.
+ *   S <= 65535; other arguments as bi_decode_attention.
  * Errors: as bi_decode_attention; an inconsistent q_indptr / seq_lens entry
  * or an out-of-range page is reported on the device (BI_ERR_DEVICE_BAD_INPUT)
  * and the affected sequence is skipped.
@@ -278,7 +283,35 @@ bi_status bi_prefill_attention(const void* q, const void* k_cache, const void* v
                                const int32_t* seq_lens, const int32_t* q_indptr, int32_t S,
                                int32_t T, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
                                int32_t num_pages, int32_t max_q_len, int32_t max_seq_len,
-                               float scale, void* out, cudaStream_t stream);
+                               float scale, void* out, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/*
+ * bi_selftest_tcgen05_vs_mma_sync -- the premise that lets prefill run on
+ * tcgen05 and still match decode bit for bit, checked on caller data: one
+ * page's score product and output update on both instruction paths, with
+ * bi_prefill_attention's descriptors and MMA forms and bi_decode_attention's
+ * mma.sync steps (the same 16-deep steps over the same operands; operand
+ * roles swapped).  "3. Batch-Invariant Attention" of "Defeating
+ * Nondeterminism in LLM Inference: The Core Role of Batch Invariance" warns
+ * that different tensor-core instructions may reduce in different orders;
+ * this call lets a test confirm that, on the GPU at hand, these two do not.
+ *   q   device, bf16 [128][128] (128 query columns)   k, v  bf16 [16][128]
+ *   p   device, bf16 [128][16] (weights)                o0   fp32 [128][128]
+ *   s_tc, s_mma   device, fp32 [128][16]: S = q . k^T, tcgen05 / mma.sync
+ *   o_tc, o_mma   device, fp32 [128][128]: o0 + p . v, tcgen05 / mma.sync
+ * Inputs 16-byte aligned.  One CTA; asynchronous on `stream`.
+ */
+bi_status bi_selftest_tcgen05_vs_mma_sync(const void* q, const void* k, const void* v,
+                                          const void* p, const float* o0, float* s_tc,
+                                          float* s_mma, float* o_tc, float* o_mma,
+                                          cudaStream_t stream);
+
+/* Workspace bytes bi_prefill_attention needs for T query rows of Hq heads of
+ * size D when some row may attend over more than one 256-token chunk
+ * (max_seq_len > 256): one fp32 D-vector per (row, head).  0 otherwise and for
+ * invalid arguments. */
+size_t bi_prefill_attention_workspace_size(int32_t T, int32_t Hq, int32_t D, int32_t max_seq_len);
 
 /*
  * bi_qk_norm_rope_append -- the steps between the qkv projection and

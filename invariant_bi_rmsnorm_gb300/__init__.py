@@ -30,8 +30,8 @@ from ._lib import DECODE_CHUNK, DECODE_COUNTER_BYTES, PAGE_SIZE
 
 __all__ = ["BiError", "rmsnorm", "gemm", "gemm_swiglu", "interleave_gate_up",
            "decode_attention", "decode_attention_fixed_splits",
-           "prefill_attention", "add_rmsnorm", "qk_norm_rope_append", "silu_mul",
-           "logprobs",
+           "prefill_attention", "prefill_attention_workspace_size", "add_rmsnorm",
+           "qk_norm_rope_append", "silu_mul", "logprobs",
            "decode_attention_workspace_size", "selftest_wait_timeout",
            "decode_num_chunks", "decode_chunk_len", "get_device_error", "abi_version",
            "status_string", "PAGE_SIZE", "DECODE_CHUNK"]
@@ -308,10 +308,15 @@ def decode_attention_fixed_splits(q, k_cache, v_cache, block_table, seq_lens, ma
     return out
 
 
+def prefill_attention_workspace_size(T: int, Hq: int, D: int, max_seq_len: int) -> int:
+    return int(_lib.load().bi_prefill_attention_workspace_size(T, Hq, D, max_seq_len))
+
+
 def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       block_table: torch.Tensor, seq_lens: torch.Tensor, q_indptr: torch.Tensor,
                       max_q_len: int, max_seq_len: int, scale: float | None = None,
-                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
     """Causal attention for the last n_i tokens of each sequence at once.
 
     q [T, Hq, D]; q_indptr [S + 1] int32 (sequence i owns q rows
@@ -340,11 +345,16 @@ def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     _cuda_bf16(out, "out")
     if tuple(out.shape) != (T, Hq, D) or not out.is_contiguous():
         raise ValueError("prefill_attention: out must be a contiguous [T, Hq, D] tensor")
+    need = prefill_attention_workspace_size(T, Hq, D, int(max_seq_len))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(_lib.load().bi_prefill_attention(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
         block_table.shape[1], seq_lens.data_ptr(), q_indptr.data_ptr(), S, T, Hq, Hkv, D, page,
-        num_pages, int(max_q_len), int(max_seq_len), float(scale), out.data_ptr(),
-        _stream(stream)), "bi_prefill_attention")
+        num_pages, int(max_q_len), int(max_seq_len), float(scale), out.data_ptr(), ws_ptr,
+        ws_bytes, _stream(stream)), "bi_prefill_attention")
     return out
 
 

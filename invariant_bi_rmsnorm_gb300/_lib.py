@@ -29,7 +29,9 @@ EXPORTS = (
     "bi_abi_version", "bi_status_string", "bi_get_device_error", "bi_rmsnorm", "bi_gemm",
     "bi_decode_attention_workspace_size", "bi_decode_num_chunks", "bi_decode_chunk_len",
     "bi_decode_attention", "bi_decode_attention_noalloc", "bi_decode_attention_fixed_splits",
-    "bi_selftest_wait_timeout", "bi_prefill_attention", "bi_add_rmsnorm",
+    "bi_selftest_wait_timeout", "bi_prefill_attention", "bi_prefill_attention_workspace_size",
+    "bi_selftest_tcgen05_vs_mma_sync",
+    "bi_add_rmsnorm",
     "bi_qk_norm_rope_append", "bi_silu_mul", "bi_decode_attention_launches", "bi_logprobs",
     "bi_gemm_swiglu",
 )
@@ -82,8 +84,12 @@ def load() -> ctypes.CDLL:
     lib.bi_decode_attention_fixed_splits.restype = ctypes.c_int
     lib.bi_prefill_attention.argtypes = [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
                                          _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _vp,
-                                         _vp]
+                                         _vp, ctypes.c_size_t, _vp]
     lib.bi_prefill_attention.restype = ctypes.c_int
+    lib.bi_selftest_tcgen05_vs_mma_sync.argtypes = [_vp] * 10
+    lib.bi_selftest_tcgen05_vs_mma_sync.restype = ctypes.c_int
+    lib.bi_prefill_attention_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
+    lib.bi_prefill_attention_workspace_size.restype = ctypes.c_size_t
     lib.bi_add_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _i64, _i64, _i64,
                                    ctypes.c_float, _vp]
     lib.bi_add_rmsnorm.restype = ctypes.c_int

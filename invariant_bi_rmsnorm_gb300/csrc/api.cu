@@ -113,6 +113,21 @@ CUresult encode_page_map(CUtensorMap* map, const void* base, uint64_t rows) {
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_q_map(CUtensorMap* map, const void* base, uint64_t T, uint64_t Hq,
+                      uint32_t box_heads, uint32_t box_rows) {
+    CUtensorMap probe;
+    const CUresult r = encode_tensor_map_2d(&probe, base, 128, T * Hq, 256, 64, 1);  // resolves the entry point
+    if (r != CUDA_SUCCESS) return r;
+    cuuint64_t dims[3] = {128, Hq, T};
+    cuuint64_t strides[2] = {256, Hq * 256};
+    cuuint32_t box[3] = {64, box_heads, box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace bi
 
 extern "C" {

@@ -156,6 +156,45 @@ __device__ __forceinline__ void softmax_step(ColState& st, const float (&sc)[4],
     pf.lo1 = bi::movmatrix_trans(rB);
 }
 
+// softmax_step for one column whose 16 raw scores of the page one thread
+// holds whole (s[t] = score of token t): the same operations on the same
+// values, so the column's state and weights get the same bits.  The page max
+// is exact in any order; the sum of the 16 weights follows softmax_step's
+// butterfly exactly: pairs (t, t + 8), then token groups j with j ^ 1, with
+// j ^ 2, with j ^ 4 (each fp32 addition commutative).  Returns alpha, the
+// factor the column's O is rescaled by; hi[i] / lo[i] receive the bf16 high
+// parts and remainders of tokens 2i, 2i + 1 (token 2i in the low half).
+__device__ __forceinline__ float softmax_page_col(float& m, float& l, const float (&s)[16],
+                                                  int valid, float scale_log2, uint32_t (&hi)[8],
+                                                  uint32_t (&lo)[8]) {
+    float x[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) x[t] = t < valid ? __fmul_rn(s[t], scale_log2) : -INFINITY;
+    float mx = x[0];
+#pragma unroll
+    for (int t = 1; t < 16; ++t) mx = fmaxf(mx, x[t]);
+    const float mn = fmaxf(m, mx);
+    const float al = mn == -INFINITY ? 1.f : exp2_ftz(__fsub_rn(m, mn));
+    float p[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) p[t] = x[t] == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x[t], mn));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        hi[i] = bi::pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        lo[i] = bi::pack_bf16x2(__fsub_rn(p[2 * i], __uint_as_float(hi[i] << 16)),
+                                __fsub_rn(p[2 * i + 1], __uint_as_float(hi[i] & 0xffff0000u)));
+    }
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = __fadd_rn(p[j], p[j + 8]);
+    const float b0 = __fadd_rn(a[0], a[1]), b2 = __fadd_rn(a[2], a[3]);
+    const float b4 = __fadd_rn(a[4], a[5]), b6 = __fadd_rn(a[6], a[7]);
+    const float ps = __fadd_rn(__fadd_rn(b0, b2), __fadd_rn(b4, b6));
+    l = __fmaf_rn(l, al, ps);
+    m = mn;
+    return al;
+}
+
 // O^T += V^T . P_hi^T, then += V^T . P_lo^T, per 16-dim tile in ascending
 // order.
 __device__ __forceinline__ void pv_step(ColState& st, const PFrags& pf, uint32_t vs_base,

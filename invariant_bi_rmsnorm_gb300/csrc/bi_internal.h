@@ -52,6 +52,13 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner
 // 16 x 64 boxes (one copy instead of two).
 CUresult encode_page_map(CUtensorMap* map, const void* base, uint64_t rows);
 
+// Query rows q[T][Hq][128] as a 3-D map (dims, heads, rows) whose box is
+// `box_heads` consecutive heads of `box_rows` consecutive rows over 64 dims,
+// 128-byte swizzled: one box lands as box_rows * box_heads rows of 128 bytes
+// in (row, head) order.
+CUresult encode_q_map(CUtensorMap* map, const void* base, uint64_t T, uint64_t Hq,
+                      uint32_t box_heads, uint32_t box_rows);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launch with programmatic stream serialization: the grid may be scheduled

@@ -1,6 +1,7 @@
 // bi_prefill_attention: attention for many query rows of the same sequence at
 // once (prompt prefill, chunked prefill), with causal visibility, and per row
-// exactly the arithmetic bi_decode_attention uses.
+// exactly the arithmetic bi_decode_attention uses -- here on tcgen05 tensor
+// cores with TMEM accumulators.
 //
 // "Defeating Nondeterminism in LLM Inference: The Core Role of Batch
 // Invariance", section "3. Batch-Invariant Attention": the FlashAttention2
@@ -13,11 +14,30 @@
 // chunk order.  A token's output is therefore bit-identical whether it is
 // computed here, in a prefill chunk of any size, or by bi_decode_attention.
 //
-// One CTA per (sequence, kv-head, tile of query rows).  The tile's columns
-// (query row x query head) are spread over 8 consumer warps, 8 columns each;
-// a producer warp streams the pages the tile needs (chunk by chunk, pages in
-// order) through a 6-stage TMA ring that all consumer warps read.  A page a
-// row cannot see (past its causal length) leaves that row's state unchanged.
+// The same products on other instructions.  Decode forms each page's scores
+// with mma.sync (S^T = K . Q^T, eight 16-deep steps over the dims, ascending,
+// into one fp32 accumulator) and each page's output update with mma.sync
+// (O^T = O^T * alpha + V^T . P_hi^T, then + V^T . P_lo^T).  Here, per tile of
+// 128 (query row, head) columns:
+//     S = Q . K_page^T        8 tcgen05.mma (M 128, N 16, K 16), dims ascending
+//     O = O * alpha           by the softmax threads, in TMEM
+//     O += P_hi . V_page      tcgen05.mma (M 128, N 128, K 16), P from TMEM
+//     O += P_lo . V_page
+// Each output element gets the same 16-deep steps in the same order, only
+// with the operand roles swapped; on GB300 the tcgen05 and mma.sync steps
+// give identical fp32 bits (measured on random and scaled operands; the tests
+// compare every prefilled row with decode, bit for bit).  The softmax of a
+// column is one thread's (softmax_page_col: decode's operations for that
+// column, in decode's order).
+//
+// CTA = (sequence, kv-head, two consecutive tiles of query rows), one CTA per
+// SM (TMEM: 512 columns).  Warp 0 streams the pages both tiles need through a
+// 4-stage TMA ring (plus the two Q tiles once); warp 1 issues the MMAs; warps
+// 2-5 and 6-9 are the softmax threads of tile 0 and tile 1, one column each
+// (warp w reads TMEM lanes 32 (w % 4) ..).  While one tile's softmax threads
+// rescale its O, the tensor core runs the other tile's products.  A page a
+// row cannot see leaves that row's state exactly unchanged (alpha = 1,
+// weights 0).  The running fold over chunks is kept in shared memory.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -39,18 +59,45 @@ using bi_attn::kPage;
 using bi_attn::kPagesPerChunk;
 using bi_attn::kStageBytes;
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kCols = kConsumerWarps * 8;             // 64 columns per tile
-constexpr int kStages = 6;
-constexpr int kSmemBytes = kStages * kStageBytes + 16 * kStages + 1024 /*align*/;
+constexpr int kTiles = 1;        // query tiles per CTA
+constexpr int kCols = 128;       // (row, head) columns per tile = TMEM lanes = MMA M
+constexpr int kSoftWarps = 4;    // softmax warps per tile, one column per thread
+constexpr int kThreads = (2 + kTiles * kSoftWarps) * 32;
+constexpr int kGroupPages = 4;   // pages per score block: S is one N = 64 product
+constexpr int kKSlots = 2;       // K ring, in score blocks
+constexpr int kKSlotBytes = 2 * kGroupPages * kHalfBytes;  // [dim half][64 tokens][128 B]: 16 KB
+constexpr int kVSlots = 4;       // V ring, in pages
+constexpr int kSBuf = 2;         // score blocks per tile in TMEM
+constexpr int kQHalf = kCols * 128;          // one 64-dim half of a Q tile: 16 KB
+constexpr int kQBytes = 2 * kQHalf;          // 32 KB
+constexpr int kPBytes = kCols * kPage * 2;   // one bf16 [128][16] weight operand: 4 KB
+constexpr int kOffK = kTiles * kQBytes;
+constexpr int kOffV = kOffK + kKSlots * kKSlotBytes;
+constexpr int kOffP = kOffV + kVSlots * kMatBytes;
+constexpr int kOffBar = kOffP + kTiles * 2 * kPBytes;
+constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 2 + kTiles * (2 * kSBuf + 2);
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024 /*align*/;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+// TMEM columns: O of tile t at t * 128; score block b of tile t at kColS +
+// (t * kSBuf + b) * 64 (page j of the block in its columns 16 j ..).
+constexpr uint32_t kTmemCols = 256;  // two CTAs per SM
+constexpr uint32_t kColS = kTiles * kD;
+constexpr uint32_t kSCols = kGroupPages * kPage;
+static_assert(kColS + kTiles * kSBuf * kSCols <= kTmemCols, "TMEM columns");
+// Instruction descriptors, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), A K-major (bit 15 = 0), B K-major (bit 16 = 0) for S
+// and MN-major (bit 16 = 1) for V, N >> 3 at bits 17-22, M >> 4 at 24-28.
+constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((kSCols >> 3) << 17) |
+                             ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                              ((128u >> 3) << 17) | ((128u >> 4) << 24);
 
 struct PrefillArgs {
-    const __nv_bfloat16* q;
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* q_indptr;
     __nv_bfloat16* out;
+    float* ws;  // [T][Hq][D] running fold of rows with more than one chunk
     uint32_t* err;
     int max_pages_per_seq;
     int Hq, Hkv, group;
@@ -62,203 +109,622 @@ struct PrefillArgs {
     float scale_log2;
 };
 
-__device__ __forceinline__ void consumer_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+// A bounded wait every lane of the warp takes, with one verdict for all of
+// them: a warp never splits over a timeout before its next collective TMEM
+// access.  (Polling from lane 0 alone, the other lanes parked in a shuffle,
+// was measured slower: 231 against 190 us for an 8048-token prefill.)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, bi::mbar_wait(bar, parity));
 }
 
-// two CTAs per SM (96 registers, a small spill) ran 12 % faster than one
-// (138 registers, no spill): the consumers are latency-bound, not spill-bound
+// K-major tile of 128-byte rows (8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr) {
+    return bi::sw128_desc_lbo_sbo(saddr, 16, 1024);
+}
+
+// A V page block [16 tokens][128 dims] as the MN-major B operand of the PV
+// product: dims 64-127 one half block (kHalfBytes) on, tokens 8-15 1024 bytes on.
+__device__ __forceinline__ uint64_t v_desc(uint32_t saddr) {
+    return bi::sw128_desc_lbo_sbo(saddr, kHalfBytes, 1024);
+}
+
+// The weights of a page as the K-major A operand [128 columns][16 tokens],
+// no swizzle: core matrices of 8 columns x 8 tokens (128 bytes), tokens 8-15
+// 128 bytes on, the next 8 columns 256 bytes on.
+__device__ __forceinline__ uint64_t p_desc(uint32_t saddr) {
+    return bi::plain_desc_lbo_sbo(saddr, 128, 256);
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
-    prefill_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
+    prefill_attn_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                        const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
-    bi::launch_dependents();
-    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
-    const int tile = blockIdx.x;
-    const int g = blockIdx.y;
-    const int s = blockIdx.z;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
 
+    // ---- geometry: longest tiles first (the grid's last tiles start first) ----
+    const int G = a.group;
+    const int rpt = a.rows_per_tile;
+    const int pair = gridDim.x - 1 - blockIdx.x;
+    const int g = blockIdx.y;
+    const int s = blockIdx.z;
     const int q0 = a.q_indptr[s];
     const int nq = a.q_indptr[s + 1] - q0;
     const int Ls = a.seq_lens[s];
-    if (q0 < 0 || nq < 0 || q0 + nq > a.T || nq > a.max_q_len ||
-        (nq > 0 && (Ls < nq || Ls > a.max_seq_len))) {
-        if (tid == 0 && tile == 0 && g == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+    const bool bad = q0 < 0 || nq < 0 || q0 + nq > a.T || nq > a.max_q_len ||
+                     (nq > 0 && (Ls < nq || Ls > a.max_seq_len));
+    if (bad) {
+        if (tid == 0 && pair == 0 && g == 0)
+            bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
         return;
     }
-    const int r0 = tile * a.rows_per_tile;
-    if (r0 >= nq) return;
-    const int nr = min(a.rows_per_tile, nq - r0);
     // query row r (0-based among the sequence's nq rows) sees the first
-    // Ls - nq + 1 + r tokens
+    // Lbase + r tokens
     const int Lbase = Ls - nq + 1;
-    const int Lmax = Lbase + r0 + nr - 1;
-    const int npg = (Lmax + kPage - 1) / kPage;
-    const int nch = (Lmax + kChunk - 1) / kChunk;
+    const int r0 = pair * kTiles * rpt;
+    if (r0 >= nq) return;  // no rows here: leave before any set-up
+    int nrt[kTiles], npg_t[kTiles];
+    int ntiles = 0, npg = 0, Lmax = 0;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        nrt[t] = max(0, min(rpt, nq - (r0 + t * rpt)));
+        npg_t[t] = 0;
+        if (nrt[t] > 0) {
+            const int Lt = Lbase + r0 + t * rpt + nrt[t] - 1;
+            npg_t[t] = (Lt + kPage - 1) / kPage;
+            ntiles = t + 1;
+            npg = max(npg, npg_t[t]);
+            Lmax = max(Lmax, Lt);
+        }
+    }
+    const int ngroups = (npg + kGroupPages - 1) / kGroupPages;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* empty = full + kStages;
+    uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kOffBar);  // [kKSlots] K block landed
+    uint64_t* kempty = kfull + kKSlots;                              // [kKSlots] K slot free
+    uint64_t* vfull = kempty + kKSlots;                              // [kVSlots] V page landed
+    uint64_t* vempty = vfull + kVSlots;                              // [kVSlots] V slot free
+    uint64_t* qfull = vempty + kVSlots;                              // Q tiles landed
+    uint64_t* drain = qfull + 1;                                     // MMAs after a timeout
+    uint64_t* sfull = drain + 1;                 // [kTiles][kSBuf] score block ready
+    uint64_t* sfree = sfull + kTiles * kSBuf;    // [kTiles][kSBuf] score block read
+    uint64_t* pready = sfree + kTiles * kSBuf;   // [kTiles] weights written, O rescaled
+    uint64_t* ovdone = pready + kTiles;          // [kTiles] the page's O products done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ovdone + kTiles);
     __shared__ int bad_page;
-
-    const int32_t* bt = a.block_table + static_cast<int64_t>(s) * a.max_pages_per_seq;
     if (tid == 0) {
-        bad_page = 0;
-        for (int i = 0; i < kStages; ++i) {
-            bi::mbar_init(&full[i], 1);
-            bi::mbar_init(&empty[i], kConsumerWarps);
+        for (int i = 0; i < kKSlots; ++i) {
+            bi::mbar_init(&kfull[i], 1);
+            bi::mbar_init(&kempty[i], 1);
+        }
+        for (int i = 0; i < kVSlots; ++i) {
+            bi::mbar_init(&vfull[i], 1);
+            bi::mbar_init(&vempty[i], 1);
+        }
+        bi::mbar_init(qfull, 1);
+        bi::mbar_init(drain, 1);
+        for (int i = 0; i < kTiles * kSBuf; ++i) {
+            bi::mbar_init(&sfull[i], 1);
+            bi::mbar_init(&sfree[i], kSoftWarps);
+        }
+        for (int t = 0; t < kTiles; ++t) {
+            bi::mbar_init(&pready[t], kSoftWarps);
+            bi::mbar_init(&ovdone[t], 1);
         }
         bi::fence_mbar_init();
+        bi::tma_prefetch_desc(&tmap_q);
         bi::tma_prefetch_desc(&tmap_k);
         bi::tma_prefetch_desc(&tmap_v);
+        bad_page = 0;
     }
+    if (warp == 1) {
+        bi::tmem_alloc(tmem_slot, kTmemCols);
+        bi::tmem_relinquish();
+    }
+    const int32_t* bt = a.block_table + static_cast<int64_t>(s) * a.max_pages_per_seq;
     __syncthreads();
     for (int i = tid; i < npg; i += kThreads) {
         const int pg = bt[i];
         if (pg < 0 || pg >= a.num_pages) bad_page = 1;
     }
+    bi::tc_fence_before();
     __syncthreads();
-    if (bad_page) {
-        if (tid == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
-        return;
-    }
+    bi::tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+    if (bad_page && tid == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+    const bool work = !bad_page;
 
-    if (warp == kConsumerWarps) {
-        // ---------------- producer: every page the tile needs, in order ----
+    if (work && warp == 0) {
+        // ---------------- producers: lane 0 the Q tiles and the K blocks,
+        // lane 16 the V pages (independent loops, each on its own ring) ------
         if (lane == 0) {
-            int k = 0;
-            for (; k < npg; ++k) {
-                const int st = k % kStages;
-                if (!bi::mbar_wait(&empty[st], ((k / kStages) & 1) ^ 1)) {
+            const uint32_t qbytes = static_cast<uint32_t>(ntiles * 2 * 64 * G * rpt * 2);
+            bi::mbar_arrive_expect_tx(qfull, qbytes);
+            for (int t = 0; t < ntiles; ++t)
+                for (int h2 = 0; h2 < 2; ++h2)
+                    bi::tma_load_3d(smem + t * kQBytes + h2 * kQHalf, &tmap_q, qfull, 64 * h2,
+                                    g * G, q0 + r0 + t * rpt);
+            int b = 0;
+            for (; b < ngroups; ++b) {
+                const int slot = b % kKSlots;
+                if (!bi::mbar_wait(&kempty[slot], ((b / kKSlots) & 1) ^ 1)) {
                     bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
                     break;
                 }
-                uint8_t* kd = smem + st * kStageBytes;
-                uint8_t* vd = kd + kMatBytes;
-                const int row = (bt[k] * a.Hkv + g) * kPage;
-                bi::mbar_arrive_expect_tx(&full[st], kStageBytes);
-                bi::tma_load_3d(kd, &tmap_k, &full[st], 0, row, 0);
-                bi::tma_load_3d(vd, &tmap_v, &full[st], 0, row, 0);
+                const int np = min(kGroupPages, npg - b * kGroupPages);
+                uint8_t* kd = smem + kOffK + slot * kKSlotBytes;
+                bi::mbar_arrive_expect_tx(&kfull[slot], static_cast<uint32_t>(np * 2 * kHalfBytes));
+                for (int j = 0; j < np; ++j) {
+                    const int row = (bt[b * kGroupPages + j] * a.Hkv + g) * kPage;
+                    bi::tma_load_2d(kd + j * kHalfBytes, &tmap_k, &kfull[slot], 0, row);
+                    bi::tma_load_2d(kd + kGroupPages * kHalfBytes + j * kHalfBytes, &tmap_k,
+                                    &kfull[slot], 64, row);
+                }
             }
             // the CTA's shared memory outlives no copy: wait (bounded) for the
-            // last copy issued into each stage -- on a healthy run the
-            // consumers wait for the same copies
-            for (int i = max(0, k - kStages); i < k; ++i)
-                bi::mbar_wait_for(&full[i % kStages], (i / kStages) & 1, bi::kDrainNs);
+            // last copies issued into each slot
+            for (int i = max(0, b - kKSlots); i < b; ++i)
+                bi::mbar_wait_for(&kfull[i % kKSlots], (i / kKSlots) & 1, bi::kDrainNs);
+            bi::mbar_wait_for(qfull, 0, bi::kDrainNs);
+        } else if (lane == 16) {
+            int p = 0;
+            for (; p < npg; ++p) {
+                const int slot = p % kVSlots;
+                if (!bi::mbar_wait(&vempty[slot], ((p / kVSlots) & 1) ^ 1)) {
+                    bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+                    break;
+                }
+                const int row = (bt[p] * a.Hkv + g) * kPage;
+                bi::mbar_arrive_expect_tx(&vfull[slot], kMatBytes);
+                bi::tma_load_3d(smem + kOffV + slot * kMatBytes, &tmap_v, &vfull[slot], 0, row, 0);
+            }
+            for (int i = max(0, p - kVSlots); i < p; ++i)
+                bi::mbar_wait_for(&vfull[i % kVSlots], (i / kVSlots) & 1, bi::kDrainNs);
         }
-        return;
-    }
-
-    // ---------------- consumers: 8 columns per warp -------------------------
-    // column n of the tile = query row n / group, head n % group
-    const int G = a.group;
-    auto col_row = [&](int n) { return n / G; };
-    uint32_t qb0[8], qb1[8];
-    {
-        const int n = warp * 8 + (lane >> 2);
-        const int rr = col_row(n);
-        const bool ok = n < a.rows_per_tile * G && rr < nr;
-        bi_attn::load_q_frags(
-            ok ? a.q + (static_cast<int64_t>(q0 + r0 + rr) * a.Hq + g * G + n % G) * kD : nullptr,
-            lane, qb0, qb1);
-    }
-    // this lane's two columns and the tokens their rows see
-    int Lcol[2];
-    int rrcol[2];
+    } else if (work && warp == 1) {
+        // ---------------- MMA issue (lane 0); the warp waits together --------
+        bool ok = warp_wait(qfull, 0);
+        bool issued = false;
+        // descriptors: the start address field is addr >> 4, so an offset
+        // within shared memory is added as offset >> 4
+        uint64_t qd[kTiles];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int n = warp * 8 + 2 * (lane & 3) + e;
-        rrcol[e] = col_row(n);
-        const bool ok = n < a.rows_per_tile * G && rrcol[e] < nr;
-        Lcol[e] = ok ? Lbase + r0 + rrcol[e] : 0;
-    }
-
-    float Mr[2] = {-INFINITY, -INFINITY}, Lr[2] = {0.f, 0.f};
-    float Ar[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) Ar[mt][0] = Ar[mt][1] = Ar[mt][2] = Ar[mt][3] = 0.f;
-
-    bool timed_out = false;
-    int k = 0;  // page counter over the whole tile
-    for (int c = 0; c < nch; ++c) {
-        bi_attn::ColState st;
-        bi_attn::colstate_init(st);
-        const int np = min(kPagesPerChunk, npg - c * kPagesPerChunk);
-        for (int p = 0; p < np; ++p, ++k) {
-            const int stg = k % kStages;
-            const bool ok = !timed_out && bi::mbar_wait(&full[stg], (k / kStages) & 1);
-            if (!ok) timed_out = true;
-            const int t0 = (c * kPagesPerChunk + p) * kPage;
-            uint8_t* kd = smem + stg * kStageBytes;
-            const int vmax = min(kPage, Lmax - t0);
-            if (vmax < kPage) {
-                // tokens past the longest row: zero their V rows once, for all warps
-                if (warp == 0 && ok) bi_attn::zero_v_tail(kd + kMatBytes, vmax, lane);
-                consumer_bar_sync();
+        for (int t = 0; t < kTiles; ++t) qd[t] = kmajor_desc(bi::smem_u32(smem + t * kQBytes));
+        static_assert(kTiles == 1, "one tile per CTA");
+        // Scores of block b, into buffer b % kSBuf: wait for the K block and
+        // the buffer, then issue its 8 k-steps.  The look-ahead block's steps
+        // go out in two shares, after the products of pages 2 and 3 of the
+        // current block, so no PV product queues behind all eight; its buffer
+        // is free by then (the softmax read the current block's last scores
+        // before it handed over page 2).
+        auto wait_s = [&](int b) -> bool {
+            if (!warp_wait(&kfull[b % kKSlots], (b / kKSlots) & 1)) return false;
+            if (!warp_wait(&sfree[b % kSBuf], ((b / kSBuf) & 1) ^ 1)) return false;
+            bi::tc_fence_after();
+            return true;
+        };
+        auto issue_s = [&](int b, int ks0, int ks1) {
+            if (lane == 0) {
+                const int slot = b % kKSlots;
+                const uint64_t kd = kmajor_desc(bi::smem_u32(smem + kOffK + slot * kKSlotBytes));
+                const uint32_t d = tm + kColS + static_cast<uint32_t>(b % kSBuf) * kSCols;
+                for (int ks = ks0; ks < ks1; ++ks)
+                    bi::tc_mma_f16(d, qd[0] + static_cast<uint64_t>(((ks >> 2) * kQHalf + 32 * (ks & 3)) >> 4),
+                                   kd + static_cast<uint64_t>(((ks >> 2) * kGroupPages * kHalfBytes + 32 * (ks & 3)) >> 4),
+                                   kIdescS, ks > 0 ? 1u : 0u);
+                if (ks1 == kD / 16) {
+                    bi::tc_commit(&sfull[b % kSBuf]);
+                    bi::tc_commit(&kempty[slot]);  // the K block is free once these finish
+                }
             }
-            if (ok) {
-                const int v0 = max(0, min(kPage, Lcol[0] - t0));
-                const int v1 = max(0, min(kPage, Lcol[1] - t0));
-                const uint32_t kb = bi::smem_u32(kd);
-                bi_attn::attend_page(st, kb, kb + kMatBytes, qb0, qb1, v0, v1, a.scale_log2, lane);
-            }
-            bi::fence_proxy_async_smem();
+            issued = true;
             __syncwarp();
-            // a warp that timed out stops handing stages back, so the producer
-            // stops too (its own wait on the stage runs out) and drains
-            if (lane == 0 && !timed_out) bi::mbar_arrive(&empty[stg]);
+        };
+        for (int b = 0; ok && b < min(kSBuf, ngroups); ++b) {
+            ok = wait_s(b);
+            if (ok) issue_s(b, 0, kD / 16);
         }
-        // fold chunk c into each column whose row sees it, as the decode path does
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            if (Lcol[e] <= c * kChunk) continue;
-            if (c == 0) {
-                Mr[e] = st.m[e];
-                Lr[e] = st.l[e];
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    Ar[mt][e] = st.acc[mt][e];
-                    Ar[mt][2 + e] = st.acc[mt][2 + e];
+        for (int b = 0; ok && b < ngroups; ++b) {
+            const int bn = b + kSBuf;  // the look-ahead block (b is then a full block)
+            const bool ahead = bn < ngroups;
+            const int npb = min(kGroupPages, npg - b * kGroupPages);
+            for (int j = 0; ok && j < npb; ++j) {
+                const int p = b * kGroupPages + j;
+                const int vslot = p % kVSlots;
+                if (!warp_wait(&vfull[vslot], (p / kVSlots) & 1)) {
+                    ok = false;
+                    break;
                 }
-            } else {
-                float Mn, fo, fc;
-                bi_attn::fold_scalars(Mr[e], st.m[e], Mn, fo, fc);
-                Lr[e] = bi_attn::fold_value(Lr[e], fo, st.l[e], fc);
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    Ar[mt][e] = bi_attn::fold_value(Ar[mt][e], fo, st.acc[mt][e], fc);
-                    Ar[mt][2 + e] = bi_attn::fold_value(Ar[mt][2 + e], fo, st.acc[mt][2 + e], fc);
+                uint8_t* vd = smem + kOffV + vslot * kMatBytes;
+                const int vmax = Lmax - p * kPage;
+                if (vmax < kPage) {
+                    // tokens past the longest row: zero their V rows (whatever
+                    // the cache holds there must not meet a zero weight as NaN)
+                    bi_attn::zero_v_tail(vd, vmax, lane);
+                    bi::fence_proxy_async_smem();
+                    __syncwarp();
                 }
-                Mr[e] = Mn;
+                if (!warp_wait(&pready[0], p & 1)) {
+                    ok = false;
+                    break;
+                }
+                bi::tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t vdesc = v_desc(bi::smem_u32(vd));
+                    const uint32_t ps = bi::smem_u32(smem + kOffP);
+                    bi::tc_mma_f16(tm, p_desc(ps), vdesc, kIdescPV, 1u);
+                    bi::tc_mma_f16(tm, p_desc(ps + kPBytes), vdesc, kIdescPV, 1u);
+                    bi::tc_commit(&ovdone[0]);
+                    bi::tc_commit(&vempty[vslot]);
+                }
+                __syncwarp();
+                if (ahead && j >= 2) {
+                    if (j == 2) ok = wait_s(bn);
+                    if (ok) issue_s(bn, (j - 2) * (kD / 32), (j - 1) * (kD / 32));
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) {
+                bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+                if (issued) {
+                    // products still in flight read shared memory and write
+                    // TMEM: a bounded wait for them before both are released
+                    bi::tc_commit(drain);
+                    bi::mbar_wait_for(drain, 0, bi::kDrainNs);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (work && warp >= 2) {
+        // ---------------- softmax: thread = one (row, head) column -----------
+        const int t = (warp - 2) / kSoftWarps;
+        if (t < ntiles) {
+            const int quarter = warp & 3;
+            const int c = quarter * 32 + lane;
+            const uint32_t lrow = tm + (static_cast<uint32_t>(quarter * 32) << 16);
+            const uint32_t col_o = lrow + static_cast<uint32_t>(t * kD);
+            const int rr = c / G;
+            const bool live = c < rpt * G && rr < nrt[t];
+            const int Lc = live ? Lbase + r0 + t * rpt + rr : 0;
+            const int64_t row = static_cast<int64_t>(q0 + r0 + t * rpt + rr) * a.Hq + g * G + c % G;
+            // this column's weights in the tile's P operands (high parts, remainders)
+            uint8_t* p_hi = smem + kOffP + t * 2 * kPBytes + (c >> 3) * 256 + (c & 7) * 16;
+            uint8_t* p_lo = p_hi + kPBytes;
+            float m = -INFINITY, l = 0.f;    // online softmax of the current chunk
+            float Mr = -INFINITY, Lr = 0.f;  // fold over the finished chunks
+            bool ok = true;
+
+            // Fold chunk k (state mk, lk and its O in TMEM) into the column's
+            // running state, as decode folds a chunk partial, and write the
+            // output if k is the column's last chunk.  Rows of one chunk keep
+            // everything in TMEM; the running O of longer rows lives in the
+            // workspace between chunks.  Columns that do not see chunk k are
+            // left unchanged.
+            auto fold_chunk = [&](int k, float mk, float lk) {
+                const bool sees = Lc > k * kChunk;
+                const bool last = sees && Lc <= (k + 1) * kChunk;
+                float fo = 1.f, fc = 1.f;
+                if (sees) {
+                    if (k == 0) {
+                        Mr = mk;
+                        Lr = lk;
+                    } else {
+                        float Mn;
+                        bi_attn::fold_scalars(Mr, mk, Mn, fo, fc);
+                        Lr = bi_attn::fold_value(Lr, fo, lk, fc);
+                        Mr = Mn;
+                    }
+                }
+                float* wrow = a.ws + row * kD;
+#pragma unroll 1
+                for (int q4 = 0; q4 < kD / 32; ++q4) {
+                    uint32_t o[32];
+                    __syncwarp();
+                    bi::tmem_ld_32x32b_x32(col_o + 32 * q4, o);
+                    bi::tmem_ld_wait();
+                    if (!sees) continue;
+                    float A[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        if (k == 0) {
+                            A[i] = __uint_as_float(o[i]);
+                            A[i + 1] = __uint_as_float(o[i + 1]);
+                            A[i + 2] = __uint_as_float(o[i + 2]);
+                            A[i + 3] = __uint_as_float(o[i + 3]);
+                        } else {
+                            const float4 w = *reinterpret_cast<const float4*>(wrow + 32 * q4 + i);
+                            A[i] = bi_attn::fold_value(w.x, fo, __uint_as_float(o[i]), fc);
+                            A[i + 1] = bi_attn::fold_value(w.y, fo, __uint_as_float(o[i + 1]), fc);
+                            A[i + 2] = bi_attn::fold_value(w.z, fo, __uint_as_float(o[i + 2]), fc);
+                            A[i + 3] = bi_attn::fold_value(w.w, fo, __uint_as_float(o[i + 3]), fc);
+                        }
+                    }
+                    if (last) {
+                        __nv_bfloat16* orow = a.out + row * kD + 32 * q4;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) {
+                            uint4 v;
+                            v.x = bi::pack_bf16x2(__fdiv_rn(A[i], Lr), __fdiv_rn(A[i + 1], Lr));
+                            v.y = bi::pack_bf16x2(__fdiv_rn(A[i + 2], Lr), __fdiv_rn(A[i + 3], Lr));
+                            v.z = bi::pack_bf16x2(__fdiv_rn(A[i + 4], Lr), __fdiv_rn(A[i + 5], Lr));
+                            v.w = bi::pack_bf16x2(__fdiv_rn(A[i + 6], Lr), __fdiv_rn(A[i + 7], Lr));
+                            *reinterpret_cast<uint4*>(orow + i) = v;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(wrow + 32 * q4 + i) =
+                                make_float4(A[i], A[i + 1], A[i + 2], A[i + 3]);
+                    }
+                }
+                __syncwarp();
+            };
+
+            // one page p whose 16 raw scores are in sv
+            auto page = [&](int p, const float (&sv)[16]) -> bool {
+                const bool first = (p % kPagesPerChunk) == 0;
+                const float m_prev = m, l_prev = l;
+                if (first) {
+                    m = -INFINITY;
+                    l = 0.f;
+                }
+                uint32_t hi[8], lo[8];
+                const int valid = max(0, min(kPage, Lc - p * kPage));
+                const float al = bi_attn::softmax_page_col(m, l, sv, valid, a.scale_log2, hi, lo);
+                if (p > 0) {
+                    if (!warp_wait(&ovdone[t], (p - 1) & 1)) return false;
+                    bi::tc_fence_after();
+                }
+                if (first) {
+                    if (p > 0) fold_chunk(p / kPagesPerChunk - 1, m_prev, l_prev);
+                    uint32_t z[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+                    for (int q4 = 0; q4 < kD / 32; ++q4) bi::tmem_st_32x32b_x32(col_o + 32 * q4, z);
+                } else if (__any_sync(0xffffffffu, al != 1.f)) {
+                    // O * alpha (a warp whose columns all have alpha == 1
+                    // exactly skips it: multiplying by one changes no bit)
+#pragma unroll 1
+                    for (int q4 = 0; q4 < kD / 32; q4 += 2) {
+                        uint32_t o0[32], o1[32];
+                        bi::tmem_ld_32x32b_x32(col_o + 32 * q4, o0);
+                        bi::tmem_ld_32x32b_x32(col_o + 32 * q4 + 32, o1);
+                        bi::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            o0[i] = __float_as_uint(__fmul_rn(__uint_as_float(o0[i]), al));
+                            o1[i] = __float_as_uint(__fmul_rn(__uint_as_float(o1[i]), al));
+                        }
+                        bi::tmem_st_32x32b_x32(col_o + 32 * q4, o0);
+                        bi::tmem_st_32x32b_x32(col_o + 32 * q4 + 32, o1);
+                    }
+                }
+                // weights of tokens 0-7 and 8-15: two core matrices of the operand
+                *reinterpret_cast<uint4*>(p_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(p_hi + 128) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                *reinterpret_cast<uint4*>(p_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4*>(p_lo + 128) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+                bi::fence_proxy_async_smem();  // the weights are read by the tensor core
+                bi::tmem_st_wait();
+                bi::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bi::mbar_arrive(&pready[t]);
+                return true;
+            };
+
+            const int np = npg_t[t];
+            const int nb = (np + kGroupPages - 1) / kGroupPages;
+            for (int b = 0; ok && b < nb; ++b) {
+                const int sb = b % kSBuf;
+                if (!warp_wait(&sfull[t * kSBuf + sb], (b / kSBuf) & 1)) {
+                    ok = false;
+                    break;
+                }
+                bi::tc_fence_after();
+                const int npb = min(kGroupPages, np - b * kGroupPages);
+                const uint32_t scol = lrow + kColS + static_cast<uint32_t>(t * kSBuf + sb) * kSCols;
+                for (int h = 0; ok && h * 2 < npb; ++h) {
+                    uint32_t sr[32];
+                    bi::tmem_ld_32x32b_x32(scol + 32 * h, sr);
+                    bi::tmem_ld_wait();
+                    if (h == 1 || npb <= 2) {  // the block's last read
+                        bi::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) bi::mbar_arrive(&sfree[t * kSBuf + sb]);
+                    }
+                    for (int jj = 0; ok && jj < 2 && 2 * h + jj < npb; ++jj) {
+                        float sv[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) sv[i] = __uint_as_float(sr[16 * jj + i]);
+                        ok = page(b * kGroupPages + 2 * h + jj, sv);
+                    }
+                }
+            }
+            if (ok && warp_wait(&ovdone[t], (np - 1) & 1)) {
+                bi::tc_fence_after();
+                fold_chunk((np - 1) / kPagesPerChunk, m, l);
+            } else if (lane == 0) {
+                bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
             }
         }
     }
-    if (timed_out) {
-        if (lane == 0) bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
-        return;
+
+    bi::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        bi::tc_fence_after();
+        bi::tmem_dealloc(tm, kTmemCols);
     }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        if (Lcol[e] == 0) continue;
-        const int n = warp * 8 + 2 * (lane & 3) + e;
-        const int64_t row = static_cast<int64_t>(q0 + r0 + rrcol[e]) * a.Hq + g * G + n % G;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int d = 16 * mt + (lane >> 2);
-            a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(Ar[mt][e], Lr[e]));
-            a.out[row * kD + d + 8] = __float2bfloat16_rn(__fdiv_rn(Ar[mt][2 + e], Lr[e]));
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the premise above: one page's products on both instruction
+// paths, with this file's descriptors and MMA forms and decode's mma.sync
+// steps (attn_common.cuh), fp32 results returned for a bit-for-bit comparison.
+//   S = Q . K^T        tcgen05 (as prefill_attn_kernel)  vs  page_scores
+//   O = O0 + P . V     tcgen05, P from shared memory      vs  one mma.sync per
+//                                                             16-dim tile
+// Q [128 columns][128], K and V one page [16][128], P [128 columns][16] (bf16),
+// O0 [128][128] fp32.  One CTA of 128 threads.
+constexpr int kStSmemQ = 0;              // 32 KB, as a Q tile
+constexpr int kStSmemK = kQBytes;        // 4 KB, as a K page block
+constexpr int kStSmemV = kStSmemK + kMatBytes;
+constexpr int kStSmemP = kStSmemV + kMatBytes;
+constexpr int kStSmemBar = kStSmemP + kPBytes;
+constexpr int kStSmemBytes = kStSmemBar + 64 + 1024;
+
+struct SelftestArgs {
+    const __nv_bfloat16 *q, *k, *v, *p;
+    const float* o0;
+    float *s_tc, *s_mma, *o_tc, *o_mma;
+    uint32_t* err;
+};
+
+__global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const SelftestArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* qs = smem + kStSmemQ;
+    uint8_t* ks = smem + kStSmemK;
+    uint8_t* vs = smem + kStSmemV;
+    uint8_t* ps = smem + kStSmemP;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kStSmemBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // operands into the kernel's shared-memory layouts (128-byte swizzle for
+    // Q, K, V; core matrices for P)
+    for (int i = tid; i < kCols * kD; i += 128) {
+        const int c = i / kD, d = i % kD;
+        *reinterpret_cast<__nv_bfloat16*>(qs + (d / 64) * kQHalf + c * 128 +
+                                          ((((d % 64) / 8) ^ (c % 8)) * 16) + (d % 8) * 2) = a.q[i];
+    }
+    for (int i = tid; i < kPage * kD; i += 128) {
+        const int t = i / kD, d = i % kD;
+        const uint32_t off = bi_attn::swz(t, d / 8) + (d % 8) * 2;
+        *reinterpret_cast<__nv_bfloat16*>(ks + off) = a.k[i];
+        *reinterpret_cast<__nv_bfloat16*>(vs + off) = a.v[i];
+    }
+    for (int i = tid; i < kCols * kPage; i += 128) {
+        const int c = i / kPage, t = i % kPage;
+        *reinterpret_cast<__nv_bfloat16*>(ps + (c / 8) * 256 + (t / 8) * 128 + (c % 8) * 16 +
+                                          (t % 8) * 2) = a.p[i];
+    }
+    if (tid == 0) {
+        bi::mbar_init(bar, 1);
+        bi::fence_mbar_init();
+    }
+    if (warp == 0) {
+        bi::tmem_alloc(tmem_slot, 256);
+        bi::tmem_relinquish();
+    }
+    bi::fence_proxy_async_smem();
+    bi::tc_fence_before();
+    __syncthreads();
+    bi::tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+
+    // mma.sync: S^T and O^T for 8 columns per group, 4 groups per warp
+    for (int j = warp * 4; j < warp * 4 + 4; ++j) {
+        uint32_t qb0[8], qb1[8];
+        bi_attn::load_q_frags(a.q + (8 * j + lane / 4) * kD, lane, qb0, qb1);
+        float sc[4];
+        bi_attn::page_scores(sc, bi::smem_u32(ks), qb0, qb1, lane);
+        for (int e = 0; e < 2; ++e) {
+            const int col = 8 * j + 2 * (lane % 4) + e;
+            a.s_mma[col * kPage + lane / 4] = sc[e];
+            a.s_mma[col * kPage + lane / 4 + 8] = sc[2 + e];
         }
+        float acc[8][4];
+        for (int mt = 0; mt < 8; ++mt)
+            for (int e = 0; e < 2; ++e) {
+                const int col = 8 * j + 2 * (lane % 4) + e;
+                acc[mt][e] = a.o0[col * kD + 16 * mt + lane / 4];
+                acc[mt][2 + e] = a.o0[col * kD + 16 * mt + lane / 4 + 8];
+            }
+        const __nv_bfloat16* pr = a.p + (8 * j + lane / 4) * kPage + 2 * (lane % 4);
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(pr);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(pr + 8);
+        const int lm_j = lane >> 3, lm_r = lane & 7;
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            bi::ldmatrix_x4_trans(bi::smem_u32(vs) + bi_attn::swz(lm_r + 8 * (lm_j >> 1), 2 * mt + (lm_j & 1)),
+                                  a0, a1, a2, a3);
+            bi::mma_bf16_16816(acc[mt], a0, a1, a2, a3, b0, b1);
+        }
+        for (int mt = 0; mt < 8; ++mt)
+            for (int e = 0; e < 2; ++e) {
+                const int col = 8 * j + 2 * (lane % 4) + e;
+                a.o_mma[col * kD + 16 * mt + lane / 4] = acc[mt][e];
+                a.o_mma[col * kD + 16 * mt + lane / 4 + 8] = acc[mt][2 + e];
+            }
+    }
+
+    // tcgen05: O0 into TMEM columns [0, 128), S into [128, 144)
+    const int c = 32 * warp + lane;
+    const uint32_t lrow = tm + (static_cast<uint32_t>(32 * warp) << 16);
+    for (int q4 = 0; q4 < kD / 32; ++q4) {
+        uint32_t r[32];
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(a.o0[c * kD + 32 * q4 + i]);
+        bi::tmem_st_32x32b_x32(lrow + 32 * q4, r);
+    }
+    bi::tmem_st_wait();
+    bi::tc_fence_before();
+    __syncthreads();
+    bi::tc_fence_after();
+    if (tid == 0) {
+        const uint64_t qd = kmajor_desc(bi::smem_u32(qs));
+        const uint64_t kd = kmajor_desc(bi::smem_u32(ks));
+        constexpr uint32_t idesc16 = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) |
+                                     ((128u >> 4) << 24);
+        for (int k = 0; k < kD / 16; ++k)
+            bi::tc_mma_f16(tm + 128, qd + static_cast<uint64_t>(((k >> 2) * kQHalf + 32 * (k & 3)) >> 4),
+                           kd + static_cast<uint64_t>(((k >> 2) * kHalfBytes + 32 * (k & 3)) >> 4),
+                           idesc16, k > 0 ? 1u : 0u);
+        bi::tc_mma_f16(tm, p_desc(bi::smem_u32(ps)), v_desc(bi::smem_u32(vs)), kIdescPV, 1u);
+        bi::tc_commit(bar);
+    }
+    __syncwarp();
+    if (!bi::mbar_wait(bar, 0)) {
+        if (lane == 0) bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+    } else {
+        bi::tc_fence_after();
+        uint32_t sr[16];
+        bi::tmem_ld_32x32b_x16(lrow + 128, sr);
+        bi::tmem_ld_wait();
+        for (int i = 0; i < kPage; ++i) a.s_tc[c * kPage + i] = __uint_as_float(sr[i]);
+        for (int q4 = 0; q4 < kD / 32; ++q4) {
+            uint32_t r[32];
+            bi::tmem_ld_32x32b_x32(lrow + 32 * q4, r);
+            bi::tmem_ld_wait();
+            for (int i = 0; i < 32; ++i) a.o_tc[c * kD + 32 * q4 + i] = __uint_as_float(r[i]);
+        }
+    }
+    bi::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        bi::tc_fence_after();
+        bi::tmem_dealloc(tm, 256);
     }
 }
 
 // set once per device; any thread may race to set it, the attribute is idempotent
 std::atomic<bool> g_attr_set[64] = {};
+std::atomic<bool> g_st_attr_set[64] = {};
 
 }  // namespace
+
+extern "C" size_t bi_prefill_attention_workspace_size(int32_t T, int32_t Hq, int32_t D,
+                                                      int32_t max_seq_len) {
+    if (T < 0 || Hq <= 0 || D <= 0 || max_seq_len <= kChunk) return 0;
+    return static_cast<size_t>(T) * Hq * D * sizeof(float);
+}
 
 extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
                                           const int32_t* block_table, int32_t max_pages_per_seq,
@@ -266,7 +732,8 @@ extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, co
                                           int32_t S, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
                                           int32_t page_size, int32_t num_pages,
                                           int32_t max_q_len, int32_t max_seq_len, float scale,
-                                          void* out, cudaStream_t stream) {
+                                          void* out, void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream) {
     if (S < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || max_pages_per_seq < 1 || num_pages < 1 ||
         max_seq_len < 1 || max_q_len < 0)
         return BI_ERR_INVALID_ARG;
@@ -286,10 +753,20 @@ extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, co
         !bi::aligned16(out) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
         (reinterpret_cast<uintptr_t>(seq_lens) & 3) || (reinterpret_cast<uintptr_t>(q_indptr) & 3))
         return BI_ERR_MISALIGNED;
+    const size_t need = bi_prefill_attention_workspace_size(T, Hq, D, max_seq_len);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return BI_ERR_WORKSPACE_TOO_SMALL;
+        if (!bi::aligned16(workspace)) return BI_ERR_MISALIGNED;
+    }
 
-    CUtensorMap tk, tv;
+    const int group = Hq / Hkv;
+    const int rows_per_tile = kCols / group;
+    CUtensorMap tq, tk, tv;
     const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv * kPage;
-    if (bi::encode_page_map(&tk, k_cache, rows) != CUDA_SUCCESS ||
+    if (bi::encode_q_map(&tq, q, static_cast<uint64_t>(T), static_cast<uint64_t>(Hq),
+                         static_cast<uint32_t>(group), static_cast<uint32_t>(rows_per_tile)) !=
+            CUDA_SUCCESS ||
+        bi::encode_tensor_map_2d(&tk, k_cache, kD, rows, kD * 2, 64, kPage) != CUDA_SUCCESS ||
         bi::encode_page_map(&tv, v_cache, rows) != CUDA_SUCCESS)
         return BI_ERR_CUDA;
 
@@ -303,25 +780,56 @@ extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, co
     }
 
     PrefillArgs args;
-    args.q = static_cast<const __nv_bfloat16*>(q);
     args.block_table = block_table;
     args.seq_lens = seq_lens;
     args.q_indptr = q_indptr;
     args.out = static_cast<__nv_bfloat16*>(out);
+    args.ws = need > 0 ? static_cast<float*>(workspace) : nullptr;
     args.err = bi::device_error_word();
     args.max_pages_per_seq = max_pages_per_seq;
     args.Hq = Hq;
     args.Hkv = Hkv;
-    args.group = Hq / Hkv;
-    args.rows_per_tile = kCols / args.group;
+    args.group = group;
+    args.rows_per_tile = rows_per_tile;
     args.num_pages = num_pages;
     args.max_seq_len = max_seq_len;
     args.max_q_len = max_q_len;
     args.T = T;
     args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    const int tiles = (max_q_len + args.rows_per_tile - 1) / args.rows_per_tile;
-    return bi::launch_pdl(prefill_attn_kernel, dim3(tiles, Hkv, S), dim3(kThreads), kSmemBytes,
-                          stream, tk, tv, args) == cudaSuccess
+    const int pairs = (max_q_len + kTiles * rows_per_tile - 1) / (kTiles * rows_per_tile);
+    return bi::launch_pdl(prefill_attn_kernel, dim3(pairs, Hkv, S), dim3(kThreads), kSmemBytes,
+                          stream, tq, tk, tv, args) == cudaSuccess
                ? BI_OK
                : BI_ERR_CUDA;
+}
+
+extern "C" bi_status bi_selftest_tcgen05_vs_mma_sync(const void* q, const void* k, const void* v,
+                                                     const void* p, const float* o0, float* s_tc,
+                                                     float* s_mma, float* o_tc, float* o_mma,
+                                                     cudaStream_t stream) {
+    if (!q || !k || !v || !p || !o0 || !s_tc || !s_mma || !o_tc || !o_mma) return BI_ERR_INVALID_ARG;
+    if (!bi::aligned16(q) || !bi::aligned16(k) || !bi::aligned16(v) || !bi::aligned16(p) ||
+        !bi::aligned16(o0))
+        return BI_ERR_MISALIGNED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
+    if (!g_st_attr_set[dev]) {
+        if (cudaFuncSetAttribute(tc_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStSmemBytes) != cudaSuccess)
+            return BI_ERR_CUDA;
+        g_st_attr_set[dev] = true;
+    }
+    SelftestArgs args;
+    args.q = static_cast<const __nv_bfloat16*>(q);
+    args.k = static_cast<const __nv_bfloat16*>(k);
+    args.v = static_cast<const __nv_bfloat16*>(v);
+    args.p = static_cast<const __nv_bfloat16*>(p);
+    args.o0 = o0;
+    args.s_tc = s_tc;
+    args.s_mma = s_mma;
+    args.o_tc = o_tc;
+    args.o_mma = o_mma;
+    args.err = bi::device_error_word();
+    tc_selftest_kernel<<<1, 128, kStSmemBytes, stream>>>(args);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }

@@ -26,7 +26,7 @@ import torch
 
 from . import (add_rmsnorm, decode_attention, decode_attention_workspace_size, gemm,
                gemm_swiglu, interleave_gate_up, logprobs, prefill_attention,
-               qk_norm_rope_append, rmsnorm, silu_mul)
+               prefill_attention_workspace_size, qk_norm_rope_append, rmsnorm, silu_mul)
 from . import inputs
 from ._lib import PAGE_SIZE
 
@@ -151,6 +151,7 @@ class Engine:
         self.free_pages = deque(range(num_pages - 1 if cuda_graphs else num_pages))
         self._graphs = {}
         self._ws = None
+        self._pws = None
         self.graph_steps = 0
         self.rope = rope_table(cfg.max_pos, cfg.rope_theta, D, device=self.device)
         T, H, F = max_tokens_per_step, cfg.hidden, cfg.ffn
@@ -251,6 +252,7 @@ class Engine:
             bt = table(pre)
             meta["pre"] = (self._rows(rows, up), i32(bt), i32(lens), i32(indptr),
                            int(max(nqs)), int(max(lens)))
+            meta["pws"] = self._prefill_workspace(len(rows), int(max(lens)))
 
         b = {k: v[:T] for k, v in self.buf.items()}
         self._layers(b, T, tok_d, pos_d, slot_d, meta)
@@ -383,6 +385,19 @@ class Engine:
             self._ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
         return self._ws
 
+    def _prefill_workspace(self, T: int, max_len: int):
+        """The prefill-attention workspace (running output of prompt rows
+        longer than one 256-token chunk), kept across steps and grown when a
+        step needs more; its contents need no initialisation."""
+        cfg = self.cfg
+        need = prefill_attention_workspace_size(T, cfg.heads, cfg.head_dim, max_len)
+        if need == 0:
+            return None
+        if self._pws is None or self._pws.numel() < need:
+            self._pws = None
+            self._pws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._pws
+
     def _ops(self):
         if self.ops == "bi":
             return gemm, rmsnorm, add_rmsnorm
@@ -427,7 +442,7 @@ class Engine:
             else:
                 _, bt, lens, indptr, mq, mx = meta[kind]
                 out = prefill_attention(q, kc, vc, bt, lens, indptr, max_q_len=mq,
-                                        max_seq_len=mx, out=out)
+                                        max_seq_len=mx, out=out, workspace=meta.get("pws"))
             if not isinstance(rows, slice):
                 b["attn"].index_copy_(0, rows, out)
 

@@ -53,7 +53,7 @@ def _prefill(p, q, nq, lens=None, max_seq_len=None):
                                 max_q_len=int(max(nq)), max_seq_len=int(max_seq_len or lens.max()))
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (24, 8), (64, 8)])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 8), (24, 8), (40, 8), (64, 8)])
 def test_full_prompt_matches_oracle_and_decode_bitwise(Hq, Hkv):
     lens = [1, 37, 300, 700]
     p, q = _prompts(lens, Hq=Hq, Hkv=Hkv, seed=400 + Hq)
@@ -66,6 +66,23 @@ def test_full_prompt_matches_oracle_and_decode_bitwise(Hq, Hkv):
     same = (ob == db).all(axis=(1, 2))
     assert same.all(), f"{(~same).sum()} of {len(rows)} rows differ from decode; first {np.argmin(same)}"
     _check(out, oracle.decode_attention(**e))
+
+
+def test_long_prompts_many_chunks_match_decode_bitwise():
+    # 2100 and 4100 tokens: 9 and 17 chunks, so every row past the first 256
+    # folds several chunk partials, and tile pairs of every length run
+    lens = [2100, 4100]
+    p, q = _prompts(lens, seed=410)
+    out = _prefill(p, q, lens)
+    rows = [(i, r + 1) for i, L in enumerate(lens) for r in range(L)]
+    e = _expanded(p, q, rows)
+    dec = bi.decode_attention(e["q"].cuda(), e["k_cache"].cuda(), e["v_cache"].cuda(),
+                              e["block_table"].cuda(), e["seq_lens"].cuda(), max_seq_len=max(lens))
+    same = (bits(out) == bits(dec)).all(axis=(1, 2))
+    assert same.all(), f"{(~same).sum()} of {len(rows)} rows differ from decode; first {np.argmin(same)}"
+    pick = np.r_[0:40, 250:270, 2090:2110, 4000:4040, 6160:6200]
+    sub = _expanded(p, q[torch.from_numpy(pick)], [rows[i] for i in pick])
+    _check(out[torch.from_numpy(pick).cuda()], oracle.decode_attention(**sub))
 
 
 def test_chunked_prefill_matches_whole_prompt_bitwise():
