@@ -145,12 +145,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     bi::launch_dependents();
     bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
 
-    // ---- geometry: longest tiles first (the grid's last tiles start first) ----
+    // ---- geometry: grid = (sequence, kv-head, tile), the tile index slowest
+    // and reversed, so the last (longest) tiles of every sequence start first ----
     const int G = a.group;
     const int rpt = a.rows_per_tile;
-    const int pair = gridDim.x - 1 - blockIdx.x;
+    const int pair = gridDim.z - 1 - blockIdx.z;
     const int g = blockIdx.y;
-    const int s = blockIdx.z;
+    const int s = blockIdx.x;
     const int q0 = a.q_indptr[s];
     const int nq = a.q_indptr[s + 1] - q0;
     const int Ls = a.seq_lens[s];
@@ -796,8 +797,9 @@ extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, co
     args.max_q_len = max_q_len;
     args.T = T;
     args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    const int pairs = (max_q_len + kTiles * rows_per_tile - 1) / (kTiles * rows_per_tile);
-    return bi::launch_pdl(prefill_attn_kernel, dim3(pairs, Hkv, S), dim3(kThreads), kSmemBytes,
+    const int tiles = (max_q_len + kTiles * rows_per_tile - 1) / (kTiles * rows_per_tile);
+    if (tiles > 65535) return BI_ERR_UNSUPPORTED_SHAPE;
+    return bi::launch_pdl(prefill_attn_kernel, dim3(S, Hkv, tiles), dim3(kThreads), kSmemBytes,
                           stream, tq, tk, tv, args) == cudaSuccess
                ? BI_OK
                : BI_ERR_CUDA;
