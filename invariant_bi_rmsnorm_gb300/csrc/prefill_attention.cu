@@ -30,14 +30,15 @@
 // column is one thread's (softmax_page_col: decode's operations for that
 // column, in decode's order).
 //
-// CTA = (sequence, kv-head, two consecutive tiles of query rows), one CTA per
-// SM (TMEM: 512 columns).  Warp 0 streams the pages both tiles need through a
-// 4-stage TMA ring (plus the two Q tiles once); warp 1 issues the MMAs; warps
-// 2-5 and 6-9 are the softmax threads of tile 0 and tile 1, one column each
-// (warp w reads TMEM lanes 32 (w % 4) ..).  While one tile's softmax threads
-// rescale its O, the tensor core runs the other tile's products.  A page a
-// row cannot see leaves that row's state exactly unchanged (alpha = 1,
-// weights 0).  The running fold over chunks is kept in shared memory.
+// CTA = (sequence, kv-head, tile of 128 (query row, head) columns), two CTAs
+// per SM (TMEM: 256 columns each).  Warp 0 loads the Q tile, then K in blocks
+// of four pages and V page by page; warp 1 issues the MMAs; warps 2-5 are the
+// softmax threads, one column each (warp w reads TMEM lanes 32 (w % 4) ..).
+// O's 128 dims are handed over in two halves, so the softmax threads rescale
+// one half while the tensor core runs the other's products.  A page a row
+// cannot see leaves that row's state exactly unchanged (alpha = 1, weights
+// 0).  Rows longer than one chunk keep their running output in a caller
+// workspace between chunks.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -74,8 +75,15 @@ constexpr int kPBytes = kCols * kPage * 2;   // one bf16 [128][16] weight operan
 constexpr int kOffK = kTiles * kQBytes;
 constexpr int kOffV = kOffK + kKSlots * kKSlotBytes;
 constexpr int kOffP = kOffV + kVSlots * kMatBytes;
-constexpr int kOffBar = kOffP + kTiles * 2 * kPBytes;
-constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 2 + kTiles * (2 * kSBuf + 2);
+constexpr int kPBufs = 2;                    // weight operands double-buffered by page
+// O's dims in two halves with their own hand-offs, so one half is rescaled
+// while the other's products run (8048-token prefill: 182 -> 165 us; four
+// parts of 32 dims were slower, 195 us: eight output MMAs per page to issue)
+constexpr int kOHalves = 2;
+constexpr int kPartCols = kD / kOHalves;     // dims per part
+static_assert(kPartCols % 32 == 0, "parts are whole 32-column TMEM loads");
+constexpr int kOffBar = kOffP + kPBufs * 2 * kPBytes;
+constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 2 + 2 * kSBuf + 2 * kOHalves;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024 /*align*/;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // TMEM columns: O of tile t at t * 128; score block b of tile t at kColS +
@@ -91,6 +99,9 @@ constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((kSCols >> 3)
                              ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                               ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// the same for one part of O's dims (N = kPartCols)
+constexpr uint32_t kIdescPVHalf = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                  ((static_cast<uint32_t>(kPartCols) >> 3) << 17) | ((128u >> 4) << 24);
 
 struct PrefillArgs {
     const int32_t* block_table;
@@ -194,9 +205,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* drain = qfull + 1;                                     // MMAs after a timeout
     uint64_t* sfull = drain + 1;                 // [kTiles][kSBuf] score block ready
     uint64_t* sfree = sfull + kTiles * kSBuf;    // [kTiles][kSBuf] score block read
-    uint64_t* pready = sfree + kTiles * kSBuf;   // [kTiles] weights written, O rescaled
-    uint64_t* ovdone = pready + kTiles;          // [kTiles] the page's O products done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ovdone + kTiles);
+    uint64_t* pready = sfree + kTiles * kSBuf;   // [kOHalves] weights written, O half rescaled
+    uint64_t* ovdone = pready + kOHalves;        // [kOHalves] the page's products on O half done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ovdone + kOHalves);
     __shared__ int bad_page;
     if (tid == 0) {
         for (int i = 0; i < kKSlots; ++i) {
@@ -213,9 +224,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             bi::mbar_init(&sfull[i], 1);
             bi::mbar_init(&sfree[i], kSoftWarps);
         }
-        for (int t = 0; t < kTiles; ++t) {
-            bi::mbar_init(&pready[t], kSoftWarps);
-            bi::mbar_init(&ovdone[t], 1);
+        for (int h = 0; h < kOHalves; ++h) {
+            bi::mbar_init(&pready[h], kSoftWarps);
+            bi::mbar_init(&ovdone[h], 1);
         }
         bi::fence_mbar_init();
         bi::tma_prefetch_desc(&tmap_q);
@@ -350,19 +361,30 @@ __global__ void __launch_bounds__(kThreads, 2)
                     bi::fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (!warp_wait(&pready[0], p & 1)) {
-                    ok = false;
-                    break;
+                // the page's products, one 64-dim half of O at a time: the
+                // softmax threads rescale one half while the other's run
+                for (int h = 0; ok && h < kOHalves; ++h) {
+                    if (!warp_wait(&pready[h], p & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    bi::tc_fence_after();
+                    if (lane == 0) {
+                        // dims [h * kPartCols, ...) of the page: their 64-dim
+                        // block, then 2 bytes per dim within it
+                        const int d0 = h * kPartCols;
+                        const uint64_t vdesc =
+                            v_desc(bi::smem_u32(vd + (d0 / 64) * kHalfBytes + (d0 % 64) * 2));
+                        const uint32_t ps = bi::smem_u32(smem + kOffP + (p % kPBufs) * 2 * kPBytes);
+                        const uint32_t o = tm + static_cast<uint32_t>(h * kPartCols);
+                        bi::tc_mma_f16(o, p_desc(ps), vdesc, kIdescPVHalf, 1u);
+                        bi::tc_mma_f16(o, p_desc(ps + kPBytes), vdesc, kIdescPVHalf, 1u);
+                        bi::tc_commit(&ovdone[h]);
+                    }
+                    __syncwarp();
                 }
-                bi::tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t vdesc = v_desc(bi::smem_u32(vd));
-                    const uint32_t ps = bi::smem_u32(smem + kOffP);
-                    bi::tc_mma_f16(tm, p_desc(ps), vdesc, kIdescPV, 1u);
-                    bi::tc_mma_f16(tm, p_desc(ps + kPBytes), vdesc, kIdescPV, 1u);
-                    bi::tc_commit(&ovdone[0]);
-                    bi::tc_commit(&vempty[vslot]);
-                }
+                if (!ok) break;
+                if (lane == 0) bi::tc_commit(&vempty[vslot]);
                 __syncwarp();
                 if (ahead && j >= 2) {
                     if (j == 2) ok = wait_s(bn);
@@ -394,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool live = c < rpt * G && rr < nrt[t];
             const int Lc = live ? Lbase + r0 + t * rpt + rr : 0;
             const int64_t row = static_cast<int64_t>(q0 + r0 + t * rpt + rr) * a.Hq + g * G + c % G;
-            // this column's weights in the tile's P operands (high parts, remainders)
-            uint8_t* p_hi = smem + kOffP + t * 2 * kPBytes + (c >> 3) * 256 + (c & 7) * 16;
-            uint8_t* p_lo = p_hi + kPBytes;
+            // this column's weights in the page's P operands (high parts,
+            // remainders), buffer p % kPBufs
+            uint8_t* p_col = smem + kOffP + (c >> 3) * 256 + (c & 7) * 16;
             float m = -INFINITY, l = 0.f;    // online softmax of the current chunk
             float Mr = -INFINITY, Lr = 0.f;  // fold over the finished chunks
             bool ok = true;
@@ -467,7 +489,31 @@ __global__ void __launch_bounds__(kThreads, 2)
                 __syncwarp();
             };
 
-            // one page p whose 16 raw scores are in sv
+            // One page p whose 16 raw scores are in sv.  The weights go to
+            // buffer p % 2 at once (its last reader, page p - 2's products,
+            // finished before page p - 1 rescaled its second half); then for
+            // each 64-dim half of O: wait for the previous page's products on
+            // it, rescale it (or zero it at a chunk start), hand it over.
+            auto rescale_half = [&](int h, float al) {
+                if (!__any_sync(0xffffffffu, al != 1.f)) return;  // alpha == 1: no bit changes
+#pragma unroll
+                for (int q = 0; q < kPartCols / 32; ++q) {
+                    uint32_t o0[32];
+                    const uint32_t cb = col_o + static_cast<uint32_t>(h * kPartCols + 32 * q);
+                    bi::tmem_ld_32x32b_x32(cb, o0);
+                    bi::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o0[i] = __float_as_uint(__fmul_rn(__uint_as_float(o0[i]), al));
+                    bi::tmem_st_32x32b_x32(cb, o0);
+                }
+            };
+            auto hand_over = [&](int h) {
+                bi::tmem_st_wait();
+                bi::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bi::mbar_arrive(&pready[h]);
+            };
             auto page = [&](int p, const float (&sv)[16]) -> bool {
                 const bool first = (p % kPagesPerChunk) == 0;
                 const float m_prev = m, l_prev = l;
@@ -478,45 +524,35 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t hi[8], lo[8];
                 const int valid = max(0, min(kPage, Lc - p * kPage));
                 const float al = bi_attn::softmax_page_col(m, l, sv, valid, a.scale_log2, hi, lo);
-                if (p > 0) {
-                    if (!warp_wait(&ovdone[t], (p - 1) & 1)) return false;
-                    bi::tc_fence_after();
-                }
+                // weights of tokens 0-7 and 8-15: two core matrices of the operand
+                uint8_t* ph = p_col + (p % kPBufs) * 2 * kPBytes;
+                *reinterpret_cast<uint4*>(ph) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(ph + 128) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                *reinterpret_cast<uint4*>(ph + kPBytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4*>(ph + kPBytes + 128) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+                bi::fence_proxy_async_smem();  // the weights are read by the tensor core
                 if (first) {
-                    if (p > 0) fold_chunk(p / kPagesPerChunk - 1, m_prev, l_prev);
+                    if (p > 0) {
+                        // the chunk that ended: both halves of its O are needed
+                        for (int h = 0; h < kOHalves; ++h)
+                            if (!warp_wait(&ovdone[h], (p - 1) & 1)) return false;
+                        bi::tc_fence_after();
+                        fold_chunk(p / kPagesPerChunk - 1, m_prev, l_prev);
+                    }
                     uint32_t z[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) z[i] = 0u;
 #pragma unroll
                     for (int q4 = 0; q4 < kD / 32; ++q4) bi::tmem_st_32x32b_x32(col_o + 32 * q4, z);
-                } else if (__any_sync(0xffffffffu, al != 1.f)) {
-                    // O * alpha (a warp whose columns all have alpha == 1
-                    // exactly skips it: multiplying by one changes no bit)
-#pragma unroll 1
-                    for (int q4 = 0; q4 < kD / 32; q4 += 2) {
-                        uint32_t o0[32], o1[32];
-                        bi::tmem_ld_32x32b_x32(col_o + 32 * q4, o0);
-                        bi::tmem_ld_32x32b_x32(col_o + 32 * q4 + 32, o1);
-                        bi::tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            o0[i] = __float_as_uint(__fmul_rn(__uint_as_float(o0[i]), al));
-                            o1[i] = __float_as_uint(__fmul_rn(__uint_as_float(o1[i]), al));
-                        }
-                        bi::tmem_st_32x32b_x32(col_o + 32 * q4, o0);
-                        bi::tmem_st_32x32b_x32(col_o + 32 * q4 + 32, o1);
-                    }
+                    for (int h = 0; h < kOHalves; ++h) hand_over(h);
+                    return true;
                 }
-                // weights of tokens 0-7 and 8-15: two core matrices of the operand
-                *reinterpret_cast<uint4*>(p_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(p_hi + 128) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-                *reinterpret_cast<uint4*>(p_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                *reinterpret_cast<uint4*>(p_lo + 128) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-                bi::fence_proxy_async_smem();  // the weights are read by the tensor core
-                bi::tmem_st_wait();
-                bi::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) bi::mbar_arrive(&pready[t]);
+                for (int h = 0; h < kOHalves; ++h) {
+                    if (!warp_wait(&ovdone[h], (p - 1) & 1)) return false;
+                    bi::tc_fence_after();
+                    rescale_half(h, al);
+                    hand_over(h);
+                }
                 return true;
             };
 
@@ -548,7 +584,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
-            if (ok && warp_wait(&ovdone[t], (np - 1) & 1)) {
+            bool last_ok = ok;
+            for (int h = 0; last_ok && h < kOHalves; ++h) last_ok = warp_wait(&ovdone[h], (np - 1) & 1);
+            if (last_ok) {
                 bi::tc_fence_after();
                 fold_chunk((np - 1) / kPagesPerChunk, m, l);
             } else if (lane == 0) {
