@@ -244,20 +244,16 @@ def test_complete_chunk_partials_stable_as_cache_grows():
         assert (np.abs(o_gpu - o_ref).max(axis=-1) <= 2 ** -6 * np.abs(o_ref).max(axis=-1) + 2 ** -12).all()
 
 
-def test_c4_full_size_sampled_parity():
-    # batch 256, lengths U[1, 8192]: 32 sampled sequences checked against the
-    # oracle, and every row of the launch is finite
-    # (the multi-gigabyte caches are drawn on the device by torch's seeded
-    # generator; the sampled sequences' pages are copied to the host for the
-    # oracle)
+def test_c4_full_size_parity():
+    # batch 1 .. 256, lengths U[1, 8192]: every row of every sequence against
+    # the oracle (the multi-gigabyte caches are drawn on the device by torch's
+    # seeded generator, then copied to the host for the oracle)
     for B in (1, 16, 128, 256):
         p = inputs.decode_problem(B, max_len=8192, seed=270 + B, device="cuda")
         out = _run(p, max_seq_len=8192)
-        assert torch.isfinite(out.float()).all()
-        rng = np.random.default_rng(B)
-        pick = np.sort(rng.choice(B, size=min(B, 32), replace=False))
-        sub = _host_subset(p, pick)
-        _check(out[torch.from_numpy(pick).cuda()], oracle.decode_attention(**sub))
+        sub = _host_subset(p, np.arange(B))
+        _check(out, oracle.decode_attention(**sub))
+        del p, sub
 
 
 def test_one_launch_folds_in_the_last_cta_and_leaves_counters_zero():

@@ -92,7 +92,7 @@ C3 = {"qkv": (6144, 4096), "o": (4096, 4096), "gate_up": (24576, 4096), "down": 
 
 
 @pytest.mark.parametrize("name", list(C3))
-def test_c3_rows_invariant_across_m_and_sampled_parity(name):
+def test_c3_rows_invariant_across_m_and_full_parity(name):
     N, K = C3[name]
     W = inputs.gemm_weight(N, K, seed=40)
     Wd = W.cuda()
@@ -106,16 +106,16 @@ def test_c3_rows_invariant_across_m_and_sampled_parity(name):
     perm = torch.randperm(4096, generator=torch.Generator().manual_seed(3))
     yp = bits(bi.gemm(xd[perm.cuda()].contiguous(), Wd))
     assert np.array_equal(yp, bb[perm.numpy()]), f"{name}: permuted batch differs"
-    # sampled parity at the full size: every output tile row/col class covered
-    rng = np.random.default_rng(4)
-    ms = np.concatenate([rng.integers(0, 4096, 600), [0, 127, 128, 4095]])
-    ns = np.concatenate([rng.integers(0, N, 600), [0, 255, 256, N - 1]])
-    ref = oracle.gemm_entries(pool, W, ms, ns)
-    got = f64(big)[ms, ns]
-    err = np.abs(got - ref)
+    # every entry of the full-size layer against the fp64 oracle
+    ref = oracle.gemm(pool, W)
+    err = np.abs(f64(big) - ref)
     assert err.max() <= 1e-2 * np.abs(ref).max()
-    absdot = oracle.gemm_entries(pool.abs(), W.abs(), ms, ns)
-    assert (err <= 2.0 ** -8 * np.abs(ref) + K * 2.0 ** -22 * absdot + 1e-30).all()
+    # fp32 accumulation over K plus the bf16 output rounding; sum_k |x||W| is
+    # only a bound factor, so numpy's fp32 product (with a small margin) serves
+    absdot = np.abs(pool.float().numpy()) @ np.abs(W.float().numpy()).T
+    bound = 2.0 ** -8 * np.abs(ref) + K * 2.0 ** -22 * (1.0 + 2.0 ** -10) * absdot + 1e-30
+    bad = np.count_nonzero(err > bound)
+    assert bad == 0, f"{name}: {bad} of {err.size} entries outside the bound"
 
 
 # ------------------------------- fused gate|up GEMM + SwiGLU (decoder MLP) ---
