@@ -19,9 +19,10 @@
 // into one fp32 accumulator) and each page's output update with mma.sync
 // (O^T = O^T * alpha + V^T . P_hi^T, then + V^T . P_lo^T).  Here, per tile of
 // 128 (query row, head) columns:
-//     S = Q . K_page^T        8 tcgen05.mma (M 128, N 16, K 16), dims ascending
+//     S = Q . K_block^T       8 tcgen05.mma (M 128, N 64, K 16) per block of
+//                             four pages, dims ascending
 //     O = O * alpha           by the softmax threads, in TMEM
-//     O += P_hi . V_page      tcgen05.mma (M 128, N 128, K 16), P from TMEM
+//     O += P_hi . V_page      tcgen05.mma (M 128, K 16), P from shared memory
 //     O += P_lo . V_page
 // Each output element gets the same 16-deep steps in the same order, only
 // with the operand roles swapped; on GB300 the tcgen05 and mma.sync steps
@@ -32,8 +33,9 @@
 //
 // CTA = (sequence, kv-head, tile of 128 (query row, head) columns), two CTAs
 // per SM (TMEM: 256 columns each).  Warp 0 loads the Q tile, then K in blocks
-// of four pages and V page by page; warp 1 issues the MMAs; warps 2-5 are the
-// softmax threads, one column each (warp w reads TMEM lanes 32 (w % 4) ..).
+// of four pages and V page by page; warp 1 issues the output products and
+// warp 6 the score products, each from one thread; warps 2-5 are the softmax
+// threads, one column each (warp w reads TMEM lanes 32 (w % 4) ..).
 // O's 128 dims are handed over in two halves, so the softmax threads rescale
 // one half while the tensor core runs the other's products.  A page a row
 // cannot see leaves that row's state exactly unchanged (alpha = 1, weights
@@ -63,7 +65,8 @@ using bi_attn::kStageBytes;
 constexpr int kTiles = 1;        // query tiles per CTA
 constexpr int kCols = 128;       // (row, head) columns per tile = TMEM lanes = MMA M
 constexpr int kSoftWarps = 4;    // softmax warps per tile, one column per thread
-constexpr int kThreads = (2 + kTiles * kSoftWarps) * 32;
+constexpr int kScoreWarp = 2 + kTiles * kSoftWarps;  // after the softmax warps
+constexpr int kThreads = (kScoreWarp + 1) * 32;
 constexpr int kGroupPages = 4;   // pages per score block: S is one N = 64 product
 constexpr int kKSlots = 2;       // K ring, in score blocks
 constexpr int kKSlotBytes = 2 * kGroupPages * kHalfBytes;  // [dim half][64 tokens][128 B]: 16 KB
@@ -83,7 +86,7 @@ constexpr int kOHalves = 2;
 constexpr int kPartCols = kD / kOHalves;     // dims per part
 static_assert(kPartCols % 32 == 0, "parts are whole 32-column TMEM loads");
 constexpr int kOffBar = kOffP + kPBufs * 2 * kPBytes;
-constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 2 + 2 * kSBuf + 2 * kOHalves;
+constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 3 + 2 * kSBuf + 2 * kOHalves;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024 /*align*/;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // TMEM columns: O of tile t at t * 128; score block b of tile t at kColS +
@@ -202,8 +205,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* vfull = kempty + kKSlots;                              // [kVSlots] V page landed
     uint64_t* vempty = vfull + kVSlots;                              // [kVSlots] V slot free
     uint64_t* qfull = vempty + kVSlots;                              // Q tiles landed
-    uint64_t* drain = qfull + 1;                                     // MMAs after a timeout
-    uint64_t* sfull = drain + 1;                 // [kTiles][kSBuf] score block ready
+    uint64_t* drain = qfull + 1;                                     // output MMAs after a timeout
+    uint64_t* drain_s = drain + 1;                                   // score MMAs after a timeout
+    uint64_t* sfull = drain_s + 1;               // [kTiles][kSBuf] score block ready
     uint64_t* sfree = sfull + kTiles * kSBuf;    // [kTiles][kSBuf] score block read
     uint64_t* pready = sfree + kTiles * kSBuf;   // [kOHalves] weights written, O half rescaled
     uint64_t* ovdone = pready + kOHalves;        // [kOHalves] the page's products on O half done
@@ -220,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         bi::mbar_init(qfull, 1);
         bi::mbar_init(drain, 1);
+        bi::mbar_init(drain_s, 1);
         for (int i = 0; i < kTiles * kSBuf; ++i) {
             bi::mbar_init(&sfull[i], 1);
             bi::mbar_init(&sfree[i], kSoftWarps);
@@ -299,98 +304,54 @@ __global__ void __launch_bounds__(kThreads, 2)
                 bi::mbar_wait_for(&vfull[i % kVSlots], (i / kVSlots) & 1, bi::kDrainNs);
         }
     } else if (work && warp == 1) {
-        // ---------------- MMA issue (lane 0); the warp waits together --------
-        bool ok = warp_wait(qfull, 0);
+        // ---------------- output products (lane 0 issues; the warp waits
+        // together).  The descriptors are built before the waits: the start
+        // address field is addr >> 4, so a shared-memory offset is added as
+        // offset >> 4, and no address arithmetic sits between a hand-over and
+        // its products.
+        const uint64_t vd0 = v_desc(bi::smem_u32(smem + kOffV));
+        const uint64_t pd0 = p_desc(bi::smem_u32(smem + kOffP));
+        bool ok = true;
         bool issued = false;
-        // descriptors: the start address field is addr >> 4, so an offset
-        // within shared memory is added as offset >> 4
-        uint64_t qd[kTiles];
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t) qd[t] = kmajor_desc(bi::smem_u32(smem + t * kQBytes));
-        static_assert(kTiles == 1, "one tile per CTA");
-        // Scores of block b, into buffer b % kSBuf: wait for the K block and
-        // the buffer, then issue its 8 k-steps.  The look-ahead block's steps
-        // go out in two shares, after the products of pages 2 and 3 of the
-        // current block, so no PV product queues behind all eight; its buffer
-        // is free by then (the softmax read the current block's last scores
-        // before it handed over page 2).
-        auto wait_s = [&](int b) -> bool {
-            if (!warp_wait(&kfull[b % kKSlots], (b / kKSlots) & 1)) return false;
-            if (!warp_wait(&sfree[b % kSBuf], ((b / kSBuf) & 1) ^ 1)) return false;
-            bi::tc_fence_after();
-            return true;
-        };
-        auto issue_s = [&](int b, int ks0, int ks1) {
-            if (lane == 0) {
-                const int slot = b % kKSlots;
-                const uint64_t kd = kmajor_desc(bi::smem_u32(smem + kOffK + slot * kKSlotBytes));
-                const uint32_t d = tm + kColS + static_cast<uint32_t>(b % kSBuf) * kSCols;
-                for (int ks = ks0; ks < ks1; ++ks)
-                    bi::tc_mma_f16(d, qd[0] + static_cast<uint64_t>(((ks >> 2) * kQHalf + 32 * (ks & 3)) >> 4),
-                                   kd + static_cast<uint64_t>(((ks >> 2) * kGroupPages * kHalfBytes + 32 * (ks & 3)) >> 4),
-                                   kIdescS, ks > 0 ? 1u : 0u);
-                if (ks1 == kD / 16) {
-                    bi::tc_commit(&sfull[b % kSBuf]);
-                    bi::tc_commit(&kempty[slot]);  // the K block is free once these finish
-                }
+        for (int p = 0; ok && p < npg; ++p) {
+            const int vslot = p % kVSlots;
+            const uint64_t vdp = vd0 + static_cast<uint64_t>((vslot * kMatBytes) >> 4);
+            const uint64_t pdp = pd0 + static_cast<uint64_t>(((p % kPBufs) * 2 * kPBytes) >> 4);
+            if (!warp_wait(&vfull[vslot], (p / kVSlots) & 1)) {
+                ok = false;
+                break;
             }
-            issued = true;
-            __syncwarp();
-        };
-        for (int b = 0; ok && b < min(kSBuf, ngroups); ++b) {
-            ok = wait_s(b);
-            if (ok) issue_s(b, 0, kD / 16);
-        }
-        for (int b = 0; ok && b < ngroups; ++b) {
-            const int bn = b + kSBuf;  // the look-ahead block (b is then a full block)
-            const bool ahead = bn < ngroups;
-            const int npb = min(kGroupPages, npg - b * kGroupPages);
-            for (int j = 0; ok && j < npb; ++j) {
-                const int p = b * kGroupPages + j;
-                const int vslot = p % kVSlots;
-                if (!warp_wait(&vfull[vslot], (p / kVSlots) & 1)) {
+            const int vmax = Lmax - p * kPage;
+            if (vmax < kPage) {
+                // tokens past the longest row: zero their V rows (whatever
+                // the cache holds there must not meet a zero weight as NaN)
+                bi_attn::zero_v_tail(smem + kOffV + vslot * kMatBytes, vmax, lane);
+                bi::fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // the page's products, one 64-dim half of O at a time: the
+            // softmax threads rescale one half while the other's run
+#pragma unroll
+            for (int h = 0; h < kOHalves; ++h) {
+                if (!warp_wait(&pready[h], p & 1)) {
                     ok = false;
                     break;
                 }
-                uint8_t* vd = smem + kOffV + vslot * kMatBytes;
-                const int vmax = Lmax - p * kPage;
-                if (vmax < kPage) {
-                    // tokens past the longest row: zero their V rows (whatever
-                    // the cache holds there must not meet a zero weight as NaN)
-                    bi_attn::zero_v_tail(vd, vmax, lane);
-                    bi::fence_proxy_async_smem();
-                    __syncwarp();
+                bi::tc_fence_after();
+                if (lane == 0) {
+                    // dims [h * 64, h * 64 + 64): the V page's h-th 64-dim block
+                    const uint64_t vdh = vdp + static_cast<uint64_t>((h * kHalfBytes) >> 4);
+                    const uint32_t o = tm + static_cast<uint32_t>(h * kPartCols);
+                    bi::tc_mma_f16(o, pdp, vdh, kIdescPVHalf, 1u);
+                    bi::tc_mma_f16(o, pdp + static_cast<uint64_t>(kPBytes >> 4), vdh, kIdescPVHalf, 1u);
+                    bi::tc_commit(&ovdone[h]);
                 }
-                // the page's products, one 64-dim half of O at a time: the
-                // softmax threads rescale one half while the other's run
-                for (int h = 0; ok && h < kOHalves; ++h) {
-                    if (!warp_wait(&pready[h], p & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    bi::tc_fence_after();
-                    if (lane == 0) {
-                        // dims [h * kPartCols, ...) of the page: their 64-dim
-                        // block, then 2 bytes per dim within it
-                        const int d0 = h * kPartCols;
-                        const uint64_t vdesc =
-                            v_desc(bi::smem_u32(vd + (d0 / 64) * kHalfBytes + (d0 % 64) * 2));
-                        const uint32_t ps = bi::smem_u32(smem + kOffP + (p % kPBufs) * 2 * kPBytes);
-                        const uint32_t o = tm + static_cast<uint32_t>(h * kPartCols);
-                        bi::tc_mma_f16(o, p_desc(ps), vdesc, kIdescPVHalf, 1u);
-                        bi::tc_mma_f16(o, p_desc(ps + kPBytes), vdesc, kIdescPVHalf, 1u);
-                        bi::tc_commit(&ovdone[h]);
-                    }
-                    __syncwarp();
-                }
-                if (!ok) break;
-                if (lane == 0) bi::tc_commit(&vempty[vslot]);
+                issued = true;
                 __syncwarp();
-                if (ahead && j >= 2) {
-                    if (j == 2) ok = wait_s(bn);
-                    if (ok) issue_s(bn, (j - 2) * (kD / 32), (j - 1) * (kD / 32));
-                }
             }
+            if (!ok) break;
+            if (lane == 0) bi::tc_commit(&vempty[vslot]);
+            __syncwarp();
         }
         if (!ok) {
             if (lane == 0) {
@@ -400,6 +361,48 @@ __global__ void __launch_bounds__(kThreads, 2)
                     // TMEM: a bounded wait for them before both are released
                     bi::tc_commit(drain);
                     bi::mbar_wait_for(drain, 0, bi::kDrainNs);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (work && warp == kScoreWarp) {
+        // ---------------- score products (lane 0 issues), on their own
+        // thread so that no output product queues behind them: block b of
+        // four pages into TMEM buffer b % kSBuf once its K block has landed
+        // and the softmax threads have read the buffer's previous block.
+        static_assert(kTiles == 1, "one tile per CTA");
+        const uint64_t qd = kmajor_desc(bi::smem_u32(smem));
+        const uint64_t kd0 = kmajor_desc(bi::smem_u32(smem + kOffK));
+        bool ok = warp_wait(qfull, 0);
+        bool issued = false;
+        for (int b = 0; ok && b < ngroups; ++b) {
+            const int slot = b % kKSlots;
+            const uint64_t kd = kd0 + static_cast<uint64_t>((slot * kKSlotBytes) >> 4);
+            const uint32_t d = tm + kColS + static_cast<uint32_t>(b % kSBuf) * kSCols;
+            ok = warp_wait(&kfull[slot], (b / kKSlots) & 1) &&
+                 warp_wait(&sfree[b % kSBuf], ((b / kSBuf) & 1) ^ 1);
+            if (!ok) break;
+            bi::tc_fence_after();
+            if (lane == 0) {
+                // k-step ks covers dims 16 ks .. 16 ks + 15: 32 bytes into
+                // the rows of 64-dim half ks / 4 of Q and of the K block
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    bi::tc_mma_f16(d, qd + static_cast<uint64_t>(((ks >> 2) * kQHalf + 32 * (ks & 3)) >> 4),
+                                   kd + static_cast<uint64_t>(((ks >> 2) * kGroupPages * kHalfBytes + 32 * (ks & 3)) >> 4),
+                                   kIdescS, ks > 0 ? 1u : 0u);
+                bi::tc_commit(&sfull[b % kSBuf]);
+                bi::tc_commit(&kempty[slot]);  // the K block is free once these finish
+            }
+            issued = true;
+            __syncwarp();
+        }
+        if (!ok) {
+            if (lane == 0) {
+                bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+                if (issued) {
+                    bi::tc_commit(drain_s);
+                    bi::mbar_wait_for(drain_s, 0, bi::kDrainNs);
                 }
             }
             __syncwarp();
