@@ -7,7 +7,8 @@ checked element by element -- the fp32 accumulators, before any rounding to
 bf16 could hide a difference -- on random data and on inputs built to expose
 a different internal order or precision: products spread over a wide
 exponent range, exact cancellation, tiny (subnormal-range) products, signed
-zeros, and accumulators that dominate the products.
+zeros, accumulators that dominate the products, and a zero accumulator
+(the first page of every chunk starts from zero).
 """
 import numpy as np
 import pytest
@@ -77,11 +78,17 @@ def _case(kind, seed):
         o0[::3] = -0.0
     elif kind == "dominant_accumulator":
         o0 = o0 * 2.0 ** 24
+    elif kind == "zero_accumulator":
+        # products onto a zero accumulator (weights with exact zeros and
+        # products of both signs, so zero sums of either sign occur)
+        o0 = torch.zeros_like(o0)
+        p[:, ::2] = 0.0
+        v[3] = -0.0
     return q, k, v, p, o0
 
 
 @pytest.mark.parametrize("kind", ["random", "scaled", "wide_exponents", "cancellation", "tiny",
-                                  "signed_zeros", "dominant_accumulator"])
+                                  "signed_zeros", "dominant_accumulator", "zero_accumulator"])
 def test_tcgen05_and_mma_sync_accumulate_identically(kind):
     for seed in range(3):
         s_tc, s_mma, o_tc, o_mma = _run(*_case(kind, 700 + seed))
