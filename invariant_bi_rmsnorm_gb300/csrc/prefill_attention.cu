@@ -238,6 +238,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         bi::tma_prefetch_desc(&tmap_k);
         bi::tma_prefetch_desc(&tmap_v);
         bad_page = 0;
+        // the Q tile does not depend on the page table: its loads go out
+        // now, overlapping the page-table check below
+        const uint32_t qbytes = static_cast<uint32_t>(ntiles * 2 * 64 * G * rpt * 2);
+        bi::mbar_arrive_expect_tx(qfull, qbytes);
+        for (int t = 0; t < ntiles; ++t)
+            for (int h2 = 0; h2 < 2; ++h2)
+                bi::tma_load_3d(smem + t * kQBytes + h2 * kQHalf, &tmap_q, qfull, 64 * h2, g * G,
+                                q0 + r0 + t * rpt);
     }
     if (warp == 1) {
         bi::tmem_alloc(tmem_slot, kTmemCols);
@@ -260,12 +268,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---------------- producers: lane 0 the Q tiles and the K blocks,
         // lane 16 the V pages (independent loops, each on its own ring) ------
         if (lane == 0) {
-            const uint32_t qbytes = static_cast<uint32_t>(ntiles * 2 * 64 * G * rpt * 2);
-            bi::mbar_arrive_expect_tx(qfull, qbytes);
-            for (int t = 0; t < ntiles; ++t)
-                for (int h2 = 0; h2 < 2; ++h2)
-                    bi::tma_load_3d(smem + t * kQBytes + h2 * kQHalf, &tmap_q, qfull, 64 * h2,
-                                    g * G, q0 + r0 + t * rpt);
             int b = 0;
             for (; b < ngroups; ++b) {
                 const int slot = b % kKSlots;
@@ -598,6 +600,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
 
+    // a CTA that skipped its work still has the Q copies issued at set-up in
+    // flight: its shared memory outlives them (bounded wait)
+    if (!work && tid == 0) bi::mbar_wait_for(qfull, 0, bi::kDrainNs);
     bi::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
