@@ -512,6 +512,253 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Small-batch form of the split kernel: the same chunks, pages and per-page
+// operations, in the same order, with each chunk's page steps shared by a
+// pair of warps.  The score warp computes each page's scores
+// (bi_attn::page_scores) and hands them over through a shared-memory ring;
+// the update warp runs the online-softmax update and the output products
+// (softmax_step, pv_step) page after page.  A page's scores do not depend on
+// the previous page, so they come off the chain of dependent steps that
+// paces a single warp; the chunk's result is the same partial, bit for bit.
+// CTA = (sequence, kv-head, group of chunks); pair k of its two pairs takes
+// chunks c0 + k, c0 + k + 2, ...  Every chunk's partial goes to the workspace
+// and the last CTA of the (sequence, kv-head) to arrive folds them, as in the
+// split kernel.  Used when a launch's chunks fill less than a wave of the GPU
+// (a few sequences), where one warp per chunk leaves most of it idle.
+constexpr int kPairs = kWarps / 2;
+constexpr int kPairStages = kStages / kPairs;  // K+V pages in flight per pair: 4
+constexpr int kScoreSlots = 4;                 // pages' scores between the two warps
+constexpr int kPairSmemBytes = kStages * kStageBytes + kFoldFloats * 4 + 4 * kMaxPagesPerCta +
+                               kPairs * kScoreSlots * 32 * 16 + 8 * kPairs * 4 * kPairStages + 1024;
+
+__global__ void __launch_bounds__(kThreads)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+    bi::launch_dependents();
+    bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
+    const int cg = blockIdx.x;  // chunk group
+    const int g = blockIdx.y;
+    const int s = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int pair = warp >> 1;
+    const bool scorer = (warp & 1) == 0;
+
+    const int L = a.seq_lens[s];
+    if (L < 1 || L > a.max_seq_len) {
+        if (tid == 0 && cg == 0 && g == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+        return;
+    }
+    int ppc, nch;
+    chunk_geometry(L, 0, ppc, nch);
+    const int c0 = cg * a.chunks_per_cta;
+    if (c0 >= nch) return;
+    const int c1 = min(nch, c0 + a.chunks_per_cta);
+    const uint32_t ngroups = static_cast<uint32_t>((nch + a.chunks_per_cta - 1) / a.chunks_per_cta);
+    uint32_t* const ctr = a.counters + static_cast<int64_t>(s) * a.Hkv + g;
+    const int npg_total = (L + kPage - 1) / kPage;
+    const int pg0 = c0 * ppc;
+    const int npg_group = min(c1 * ppc, npg_total) - pg0;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float* fold_o = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+    int32_t* rows_s = reinterpret_cast<int32_t*>(fold_o + kFoldFloats);  // TMA row per page
+    float4* ring = reinterpret_cast<float4*>(rows_s + kMaxPagesPerCta);    // [pair][slot][lane]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kPairs * kScoreSlots * 32);
+    uint64_t* full = bars + pair * 4 * kPairStages;   // [kPairStages] page landed
+    uint64_t* empty = full + kPairStages;             // [kPairStages] page's products done
+    uint64_t* sfull = empty + kPairStages;            // [kScoreSlots] scores written
+    uint64_t* sempty = sfull + kScoreSlots;           // [kScoreSlots] scores read
+    float4* my_ring = ring + pair * kScoreSlots * 32;
+    __shared__ int bad_page;
+
+    if (tid == 0) {
+        bad_page = 0;
+        for (int i = 0; i < kPairs * 4 * kPairStages; ++i) bi::mbar_init(&bars[i], 1);
+        bi::fence_mbar_init();
+        bi::tma_prefetch_desc(&tmap_k);
+        bi::tma_prefetch_desc(&tmap_v);
+    }
+    __syncthreads();
+    for (int i = tid; i < npg_group; i += kThreads) {
+        const int pg = a.block_table[static_cast<int64_t>(s) * a.max_pages_per_seq + pg0 + i];
+        if (pg < 0 || pg >= a.num_pages) {
+            bad_page = 1;
+        } else {
+            rows_s[i] = (pg * a.Hkv + g) * kPage;
+        }
+    }
+    __syncthreads();
+    if (bad_page) {
+        if (tid == 0) {
+            bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+            const uint32_t now = bi::atomic_add_acq_rel_gpu(ctr, kArriveBad) + kArriveBad;
+            if ((now & 0xffffu) == ngroups) atomicExch(ctr, 0u);
+        }
+        return;
+    }
+
+    auto pages_in = [&](int c) { return min(ppc, npg_total - c * ppc); };
+    auto stage_ptr = [&](int j) { return smem + (pair * kPairStages + j % kPairStages) * kStageBytes; };
+    bool timed_out = false;
+
+    if (scorer) {
+        // ---- loads (lane 0) and page scores ----
+        int lc = c0 + pair, lp = 0, lj = 0;
+        auto issue_next = [&]() {
+            if (lc >= c1) return;
+            if (lane == 0) {
+                uint8_t* kd = stage_ptr(lj);
+                const int row = rows_s[(lc - c0) * ppc + lp];
+                uint64_t* bar = &full[lj % kPairStages];
+                bi::mbar_arrive_expect_tx(bar, kStageBytes);
+                bi::tma_load_3d(kd, &tmap_k, bar, 0, row, 0);
+                bi::tma_load_3d(kd + kMatBytes, &tmap_v, bar, 0, row, 0);
+            }
+            ++lj;
+            if (++lp >= pages_in(lc)) {
+                lc += kPairs;
+                lp = 0;
+            }
+        };
+#pragma unroll
+        for (int i = 0; i < kPairStages; ++i) issue_next();
+        uint32_t qb0[8], qb1[8];
+        {
+            const int n = lane >> 2;
+            bi_attn::load_q_frags(
+                n < a.group ? a.q + (static_cast<int64_t>(s) * a.Hq + g * a.group + n) * kD : nullptr,
+                lane, qb0, qb1);
+        }
+        int j = 0;
+        int seen = 0;  // pages whose copies this warp saw land
+        for (int c = c0 + pair; c < c1 && !timed_out; c += kPairs) {
+            const int np = pages_in(c);
+            for (int p = 0; p < np; ++p, ++j) {
+                if (!__all_sync(0xffffffffu, bi::mbar_wait(&full[j % kPairStages], (j / kPairStages) & 1))) {
+                    timed_out = true;
+                    break;
+                }
+                seen = j + 1;
+                float sc[4];
+                bi_attn::page_scores(sc, bi::smem_u32(stage_ptr(j)), qb0, qb1, lane);
+                const int slot = j % kScoreSlots;
+                if (!__all_sync(0xffffffffu, bi::mbar_wait(&sempty[slot], ((j / kScoreSlots) & 1) ^ 1))) {
+                    timed_out = true;
+                    break;
+                }
+                my_ring[slot * 32 + lane] = make_float4(sc[0], sc[1], sc[2], sc[3]);
+                __syncwarp();
+                if (lane == 0) bi::mbar_arrive(&sfull[slot]);
+                if (j >= 1) {
+                    // page j - 1's stage is free once its products are done:
+                    // the copy for page j - 1 + kPairStages goes into it (after
+                    // this page's scores are handed over, so the score warp
+                    // stays ahead of the update warp)
+                    if (!__all_sync(0xffffffffu, bi::mbar_wait(&empty[(j - 1) % kPairStages],
+                                                              ((j - 1) / kPairStages) & 1))) {
+                        timed_out = true;
+                        break;
+                    }
+                    issue_next();
+                }
+            }
+        }
+        if (timed_out && lane == 0) {
+            bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+            // copies issued and never seen to land: one more bounded wait each
+            for (int i = seen; i < lj; ++i)
+                bi::mbar_wait_for(&full[i % kPairStages], (i / kPairStages) & 1, bi::kDrainNs);
+        }
+    } else {
+        // ---- online-softmax update and output products, page after page ----
+        const int h0 = 2 * (lane & 3);
+        int j = 0;
+        for (int c = c0 + pair; c < c1 && !timed_out; c += kPairs) {
+            bi_attn::ColState st;
+            bi_attn::colstate_init(st);
+            const int np = pages_in(c);
+            for (int p = 0; p < np; ++p, ++j) {
+                const int slot = j % kScoreSlots;
+                if (!__all_sync(0xffffffffu, bi::mbar_wait(&sfull[slot], (j / kScoreSlots) & 1))) {
+                    timed_out = true;
+                    break;
+                }
+                const float4 v4 = my_ring[slot * 32 + lane];
+                const float sc[4] = {v4.x, v4.y, v4.z, v4.w};
+                __syncwarp();
+                if (lane == 0) bi::mbar_arrive(&sempty[slot]);
+                // the page's V, landed (the score warp saw the same phase)
+                if (!__all_sync(0xffffffffu, bi::mbar_wait(&full[j % kPairStages], (j / kPairStages) & 1))) {
+                    timed_out = true;
+                    break;
+                }
+                uint8_t* vd = stage_ptr(j) + kMatBytes;
+                const int valid = min(kPage, L - (c * ppc + p) * kPage);
+                if (valid < kPage) {
+                    bi_attn::zero_v_tail(vd, valid, lane);
+                    __syncwarp();
+                }
+                bi_attn::PFrags pf;
+                bi_attn::softmax_step(st, sc, valid, valid, a.scale_log2, lane, pf);
+                bi_attn::pv_step(st, pf, bi::smem_u32(vd), lane);
+                // the zeroed V tail (generic-proxy writes) is ordered before the
+                // next copy (an async-proxy write) into the same stage
+                if (valid < kPage) bi::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) bi::mbar_arrive(&empty[j % kPairStages]);
+            }
+            if (timed_out) break;
+            // chunk partial -> workspace
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = h0 + e;
+                if (h >= a.group) continue;
+                const int64_t pidx = (static_cast<int64_t>(s) * a.Hq + g * a.group + h) * a.max_chunks + c;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const int d = 16 * mt + (lane >> 2);
+                    a.ws_acc[pidx * kD + d] = st.acc[mt][e];
+                    a.ws_acc[pidx * kD + d + 8] = st.acc[mt][2 + e];
+                }
+                if (lane < 4) {
+                    a.ws_ml[pidx * 2] = st.m[e];
+                    a.ws_ml[pidx * 2 + 1] = st.l[e];
+                }
+            }
+        }
+        if (timed_out && lane == 0) bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
+    }
+
+    // ---- arrival: the last CTA of this (sequence, kv-head) folds it ------
+    __shared__ int fold_here;
+    __syncthreads();  // every warp's partial stores precede the arrival
+    if (tid == 0) {
+        const uint32_t now = bi::atomic_add_acq_rel_gpu(ctr, kArrive) + kArrive;
+        const bool last = (now & 0xffffu) == ngroups;
+        if (last) {
+            atomicExch(ctr, 0u);  // ready for the next call
+            if (now >> 16) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+        }
+        fold_here = last && (now >> 16) == 0;
+    }
+    __syncthreads();
+    if (!fold_here) return;
+    switch (a.group) {
+        case 1: fold_sequence<1>(a, s, g, nch, smem, fold_o, tid); break;
+        case 2: fold_sequence<2>(a, s, g, nch, smem, fold_o, tid); break;
+        case 3: fold_sequence<3>(a, s, g, nch, smem, fold_o, tid); break;
+        case 4: fold_sequence<4>(a, s, g, nch, smem, fold_o, tid); break;
+        case 5: fold_sequence<5>(a, s, g, nch, smem, fold_o, tid); break;
+        case 6: fold_sequence<6>(a, s, g, nch, smem, fold_o, tid); break;
+        case 7: fold_sequence<7>(a, s, g, nch, smem, fold_o, tid); break;
+        default: fold_sequence<8>(a, s, g, nch, smem, fold_o, tid); break;
+    }
+}
+
 // Fold the chunk partials of one (sequence, query head) in ascending chunk
 // order:  M' = max(M, m_c);  l' = l 2^(M-M') + l_c 2^(m_c-M');
 //         O' = O 2^(M-M') + O_c 2^(m_c-M');   out = bf16(O / l).
@@ -659,7 +906,9 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
     if (!g_attr_set[dev]) {
         if (cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
+                                 kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) != cudaSuccess)
             return BI_ERR_CUDA;
         g_attr_set[dev] = true;
     }
@@ -698,8 +947,22 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
         const int ppc_max = ceil_div(ceil_div(max_seq_len, kPage), num_splits);
         cpc = std::max(1, std::min(std::min(num_splits, kWarps), kMaxPagesPerCta / ppc_max));
     }
+    // a few sequences: their chunks, one per warp pair, need no more than one
+    // CTA per SM, so each chunk's page steps are shared by two warps
+    // (attn_pair_kernel; same operations, same order, same bits).  With two
+    // such CTAs on an SM the split kernel is faster (measured at 2 sequences).
+    const bool paired = num_splits == 0 && counted &&
+                        static_cast<int64_t>(B) * Hkv * ceil_div(max_chunks, kPairs) <=
+                            static_cast<int64_t>(bi::sm_count());
+    if (paired) cpc = kPairs;
     args.chunks_per_cta = cpc;
     const int groups = ceil_div(max_chunks, cpc);
+    if (paired) {
+        return bi::launch_pdl(attn_pair_kernel, dim3(groups, Hkv, B), dim3(kThreads), kPairSmemBytes,
+                              stream, tk, tv, args) == cudaSuccess
+                   ? BI_OK
+                   : BI_ERR_CUDA;
+    }
     if (bi::launch_pdl(attn_split_kernel, dim3(groups, Hkv, B), dim3(kThreads), kSmemBytes, stream,
                        tk, tv, args) != cudaSuccess)
         return BI_ERR_CUDA;

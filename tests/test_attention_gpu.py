@@ -82,8 +82,10 @@ def test_gqa_group_sizes(Hq, Hkv):
 @pytest.mark.parametrize("G", [1, 2, 3, 5, 8])
 def test_last_cta_fold_equals_in_cta_fold_for_every_group_size(G):
     # In a batch of 256 each sequence (up to 32 chunks) is walked and folded
-    # by one CTA; alone it is spread over up to 8 CTAs and folded by the last
-    # to arrive.  Same operations in the same order: same bits.
+    # by one CTA; alone it runs on the small-batch kernel (each chunk's pages
+    # shared by a score warp and an update warp), spread over up to 16 CTAs
+    # and folded by the last to arrive.  Same operations in the same order:
+    # same bits.
     B, Hkv = 256, 8
     p = inputs.decode_problem(B, Hq=G * Hkv, Hkv=Hkv, max_len=8192, seed=400 + G, device="cuda")
     lib = bi._lib.load()
@@ -97,6 +99,27 @@ def test_last_cta_fold_equals_in_cta_fold_for_every_group_size(G):
     sub = _host_subset(p, np.array(pick))
     rows = torch.from_numpy(full[pick].view(np.int16)).view(torch.bfloat16)
     _check(rows, oracle.decode_attention(**sub))
+
+
+@pytest.mark.parametrize("G", [4, 7])
+def test_small_batch_kernel_equals_split_kernel(G):
+    # One or two sequences take the small-batch kernel (a warp pair per
+    # chunk); the same sequences inside a batch of 64 take the split kernel
+    # (a warp per chunk).  Lengths of one chunk, of two chunks (one CTA, both
+    # pairs), and of many chunks (several CTAs and the last-CTA fold).
+    Hkv = 8
+    g = torch.Generator().manual_seed(G)
+    lens = [100, 300, 5000, 8192] + torch.randint(1, 8193, (60,), generator=g).tolist()
+    p = inputs.decode_problem(len(lens), Hq=G * Hkv, Hkv=Hkv, seq_lens=lens, seed=450 + G,
+                              spare_pages=3)
+    full = bits(_run(p, max_seq_len=8192))
+    for idx in ([0], [1], [2], [3], [1, 2]):
+        sel = torch.tensor(idx)
+        few = {k: (v[sel].contiguous() if k in ("q", "block_table", "seq_lens") else v)
+               for k, v in p.items()}
+        got = bits(_run(few, max_seq_len=8192))
+        assert np.array_equal(got, full[idx]), f"sequences {idx}"
+    bi.get_device_error()
 
 
 def test_custom_scale():
