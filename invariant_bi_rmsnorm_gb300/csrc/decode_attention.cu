@@ -26,6 +26,10 @@
 // writes bf16(O / l) and returns the counter to zero.  Which CTA arrives last
 // decides only who folds, never what is folded or in which order.  No float
 // atomics: the counter is a plain integer add.
+// Kernel 1' (pair), instead of kernel 1 for launches of a few sequences: the
+// same chunks and per-page operations with two warps per chunk (one forms
+// the scores, one runs the softmax update and the output products), every
+// chunk's partial folded by the last CTA to arrive.
 // Kernel 2 (merge), only for launches with more (sequence, kv-head) pairs
 // than the workspace has counters: the same fold as a separate kernel.
 // How many chunks a CTA walks is chosen per launch to fill the GPU; it moves
