@@ -951,13 +951,14 @@ bi_status launch_attention(const void* q, const void* k_cache, const void* v_cac
         const int ppc_max = ceil_div(ceil_div(max_seq_len, kPage), num_splits);
         cpc = std::max(1, std::min(std::min(num_splits, kWarps), kMaxPagesPerCta / ppc_max));
     }
-    // a few sequences: their chunks, one per warp pair, need no more than one
-    // CTA per SM, so each chunk's page steps are shared by two warps
-    // (attn_pair_kernel; same operations, same order, same bits).  With two
-    // such CTAs on an SM the split kernel is faster (measured at 2 sequences).
+    // a few sequences: their chunks, one per warp pair, need no more than two
+    // CTAs per SM, so each chunk's page steps are shared by two warps
+    // (attn_pair_kernel; same operations, same order, same bits).  Measured
+    // cold against the split kernel: faster at 1-2 sequences of up to 8192
+    // tokens, even or slower from 3 on.
     const bool paired = num_splits == 0 && counted &&
                         static_cast<int64_t>(B) * Hkv * ceil_div(max_chunks, kPairs) <=
-                            static_cast<int64_t>(bi::sm_count());
+                            2 * static_cast<int64_t>(bi::sm_count());
     if (paired) cpc = kPairs;
     args.chunks_per_cta = cpc;
     const int groups = ceil_div(max_chunks, cpc);
