@@ -6,7 +6,8 @@
 // tokens (rows of K and V) and 8 columns (query head x query row pairs):
 //     S^T[16 x 8] = K_page[16 x 128] . Q^T[128 x 8]       8 mma.sync, dims ascending
 //     x = S * scale * log2(e)        (tokens past a column's length -> -inf)
-//     m' = max(m, max_t x);  alpha = 2^(m - m');  p = 2^(x - m')  (fp32)
+//     m' = max_t x if it exceeds m by more than kRescaleSlack, else m;
+//     alpha = 2^(m - m') (exactly 1 when m' = m);  p = 2^(x - m')  (fp32)
 //     l' = l * alpha + sum_t p       (fixed xor-butterfly order over tokens)
 //     p = p_hi + p_lo with p_hi = bf16(p), p_lo = bf16(p - p_hi)
 //     O^T[128 x 8] = (O^T * alpha + V^T . P_hi^T) + V^T . P_lo^T   16 mma.sync
@@ -94,6 +95,14 @@ __device__ __forceinline__ void page_scores(float (&sc)[4], uint32_t ks_base,
     }
 }
 
+// The reference maximum m of a column moves only when a page's maximum
+// exceeds it by more than this many log2 units (a factor of 256): below
+// that, the page's weights stay at most 2^8 and the running sum and output
+// keep their scale -- alpha is exactly 1, so the output needs no rescaling.
+// The result is the same softmax (the final O / l does not depend on the
+// reference); only the rounding sequence is fixed differently.
+constexpr float kRescaleSlack = 8.f;
+
 // 2^x as one ex2.approx.ftz.f32 (bi::ex2_approx) on the per-page dependency
 // chain, where exp2f() takes several instructions.  Decode, prefill and the
 // chunk folds all take their exponentials from here.
@@ -117,10 +126,12 @@ __device__ __forceinline__ void softmax_step(ColState& st, const float (&sc)[4],
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
-    // a column with no visible token so far keeps m = -inf: no rescale, p = 0
-    const float al0 = mn0 == -INFINITY ? 1.f : exp2_ftz(__fsub_rn(st.m[0], mn0));
-    const float al1 = mn1 == -INFINITY ? 1.f : exp2_ftz(__fsub_rn(st.m[1], mn1));
+    // the reference moves only past the slack; a column with no visible token
+    // so far keeps m = -inf (-inf + slack is -inf): no rescale, p = 0
+    const float mn0 = mx0 > __fadd_rn(st.m[0], kRescaleSlack) ? mx0 : st.m[0];
+    const float mn1 = mx1 > __fadd_rn(st.m[1], kRescaleSlack) ? mx1 : st.m[1];
+    const float al0 = mn0 == st.m[0] ? 1.f : exp2_ftz(__fsub_rn(st.m[0], mn0));
+    const float al1 = mn1 == st.m[1] ? 1.f : exp2_ftz(__fsub_rn(st.m[1], mn1));
     const float p0 = x0 == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x0, mn0));
     const float p1 = x1 == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x1, mn1));
     const float p2 = x2 == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x2, mn0));
@@ -173,8 +184,8 @@ __device__ __forceinline__ float softmax_page_col(float& m, float& l, const floa
     float mx = x[0];
 #pragma unroll
     for (int t = 1; t < 16; ++t) mx = fmaxf(mx, x[t]);
-    const float mn = fmaxf(m, mx);
-    const float al = mn == -INFINITY ? 1.f : exp2_ftz(__fsub_rn(m, mn));
+    const float mn = mx > __fadd_rn(m, kRescaleSlack) ? mx : m;
+    const float al = mn == m ? 1.f : exp2_ftz(__fsub_rn(m, mn));
     float p[16];
 #pragma unroll
     for (int t = 0; t < 16; ++t) p[t] = x[t] == -INFINITY ? 0.f : exp2_ftz(__fsub_rn(x[t], mn));
