@@ -78,15 +78,15 @@ constexpr int kPBytes = kCols * kPage * 2;   // one bf16 [128][16] weight operan
 constexpr int kOffK = kTiles * kQBytes;
 constexpr int kOffV = kOffK + kKSlots * kKSlotBytes;
 constexpr int kOffP = kOffV + kVSlots * kMatBytes;
-constexpr int kPBufs = 2;                    // weight operands double-buffered by page
-// O's dims in two halves with their own hand-offs, so one half is rescaled
-// while the other's products run (8048-token prefill: 182 -> 165 us; four
-// parts of 32 dims were slower, 195 us: eight output MMAs per page to issue)
-constexpr int kOHalves = 2;
-constexpr int kPartCols = kD / kOHalves;     // dims per part
-static_assert(kPartCols % 32 == 0, "parts are whole 32-column TMEM loads");
+// Weight operands by page.  A page is handed to the tensor core as soon as
+// its weights are written: its products add onto O behind the previous
+// page's in the tensor pipe, so the softmax threads wait for the previous
+// page's products only when they must touch O themselves (a rescale, which
+// the reference-maximum slack makes rare, a chunk fold, the tile's end).
+// The buffers bound how far ahead of the tensor core they run.
+constexpr int kPBufs = 3;
 constexpr int kOffBar = kOffP + kPBufs * 2 * kPBytes;
-constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 3 + 2 * kSBuf + 2 * kOHalves;
+constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 3 + 2 * kSBuf + 2 * kPBufs;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024 /*align*/;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // TMEM columns: O of tile t at t * 128; score block b of tile t at kColS +
@@ -102,9 +102,6 @@ constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((kSCols >> 3)
                              ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                               ((128u >> 3) << 17) | ((128u >> 4) << 24);
-// the same for one part of O's dims (N = kPartCols)
-constexpr uint32_t kIdescPVHalf = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
-                                  ((static_cast<uint32_t>(kPartCols) >> 3) << 17) | ((128u >> 4) << 24);
 
 struct PrefillArgs {
     const int32_t* block_table;
@@ -209,9 +206,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* drain_s = drain + 1;                                   // score MMAs after a timeout
     uint64_t* sfull = drain_s + 1;               // [kTiles][kSBuf] score block ready
     uint64_t* sfree = sfull + kTiles * kSBuf;    // [kTiles][kSBuf] score block read
-    uint64_t* pready = sfree + kTiles * kSBuf;   // [kOHalves] weights written, O half rescaled
-    uint64_t* ovdone = pready + kOHalves;        // [kOHalves] the page's products on O half done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ovdone + kOHalves);
+    uint64_t* pfull = sfree + kTiles * kSBuf;    // [kPBufs] a page's weights written (O ready)
+    uint64_t* pempty = pfull + kPBufs;           // [kPBufs] that page's products done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + kPBufs);
     __shared__ int bad_page;
     if (tid == 0) {
         for (int i = 0; i < kKSlots; ++i) {
@@ -229,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             bi::mbar_init(&sfull[i], 1);
             bi::mbar_init(&sfree[i], kSoftWarps);
         }
-        for (int h = 0; h < kOHalves; ++h) {
-            bi::mbar_init(&pready[h], kSoftWarps);
-            bi::mbar_init(&ovdone[h], 1);
+        for (int i = 0; i < kPBufs; ++i) {
+            bi::mbar_init(&pfull[i], kSoftWarps);
+            bi::mbar_init(&pempty[i], 1);
         }
         bi::fence_mbar_init();
         bi::tma_prefetch_desc(&tmap_q);
@@ -331,26 +328,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                 bi::fence_proxy_async_smem();
                 __syncwarp();
             }
-            // the page's products, one 64-dim half of O at a time: the
-            // softmax threads rescale one half while the other's run
-#pragma unroll
-            for (int h = 0; h < kOHalves; ++h) {
-                if (!warp_wait(&pready[h], p & 1)) {
-                    ok = false;
-                    break;
-                }
-                bi::tc_fence_after();
-                if (lane == 0) {
-                    // dims [h * 64, h * 64 + 64): the V page's h-th 64-dim block
-                    const uint64_t vdh = vdp + static_cast<uint64_t>((h * kHalfBytes) >> 4);
-                    const uint32_t o = tm + static_cast<uint32_t>(h * kPartCols);
-                    bi::tc_mma_f16(o, pdp, vdh, kIdescPVHalf, 1u);
-                    bi::tc_mma_f16(o, pdp + static_cast<uint64_t>(kPBytes >> 4), vdh, kIdescPVHalf, 1u);
-                    bi::tc_commit(&ovdone[h]);
-                }
-                issued = true;
-                __syncwarp();
+            const int pb = p % kPBufs;
+            if (!warp_wait(&pfull[pb], (p / kPBufs) & 1)) {
+                ok = false;
+                break;
             }
+            bi::tc_fence_after();
+            if (lane == 0) {
+                // O += P_hi . V, then O += P_lo . V (N = 128: all of O's dims)
+                bi::tc_mma_f16(tm, pdp, vdp, kIdescPV, 1u);
+                bi::tc_mma_f16(tm, pdp + static_cast<uint64_t>(kPBytes >> 4), vdp, kIdescPV, 1u);
+                bi::tc_commit(&pempty[pb]);  // the page's products (and all before) done
+            }
+            issued = true;
+            __syncwarp();
             if (!ok) break;
             if (lane == 0) bi::tc_commit(&vempty[vslot]);
             __syncwarp();
@@ -495,29 +486,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             };
 
             // One page p whose 16 raw scores are in sv.  The weights go to
-            // buffer p % 2 at once (its last reader, page p - 2's products,
-            // finished before page p - 1 rescaled its second half); then for
-            // each 64-dim half of O: wait for the previous page's products on
-            // it, rescale it (or zero it at a chunk start), hand it over.
-            auto rescale_half = [&](int h, float al) {
-                if (!__any_sync(0xffffffffu, al != 1.f)) return;  // alpha == 1: no bit changes
-#pragma unroll
-                for (int q = 0; q < kPartCols / 32; ++q) {
-                    uint32_t o0[32];
-                    const uint32_t cb = col_o + static_cast<uint32_t>(h * kPartCols + 32 * q);
-                    bi::tmem_ld_32x32b_x32(cb, o0);
-                    bi::tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o0[i] = __float_as_uint(__fmul_rn(__uint_as_float(o0[i]), al));
-                    bi::tmem_st_32x32b_x32(cb, o0);
-                }
+            // buffer p % kPBufs once the page that used it last has had its
+            // products; the page is handed over at once unless O must be
+            // touched first: rescaled (some alpha of the warp not 1), or
+            // folded and zeroed at a chunk start.  Either waits for the
+            // previous page's products, which by then are the last on O.
+            auto wait_products = [&](int q) {  // page q's products (and all before) done
+                return warp_wait(&pempty[q % kPBufs], (q / kPBufs) & 1);
             };
-            auto hand_over = [&](int h) {
+            auto hand_over = [&](int pb) {
                 bi::tmem_st_wait();
                 bi::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) bi::mbar_arrive(&pready[h]);
+                if (lane == 0) bi::mbar_arrive(&pfull[pb]);
             };
             auto page = [&](int p, const float (&sv)[16]) -> bool {
                 const bool first = (p % kPagesPerChunk) == 0;
@@ -529,8 +510,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t hi[8], lo[8];
                 const int valid = max(0, min(kPage, Lc - p * kPage));
                 const float al = bi_attn::softmax_page_col(m, l, sv, valid, a.scale_log2, hi, lo);
+                const int pb = p % kPBufs;
+                if (!warp_wait(&pempty[pb], ((p / kPBufs) & 1) ^ 1)) return false;  // buffer free
                 // weights of tokens 0-7 and 8-15: two core matrices of the operand
-                uint8_t* ph = p_col + (p % kPBufs) * 2 * kPBytes;
+                uint8_t* ph = p_col + pb * 2 * kPBytes;
                 *reinterpret_cast<uint4*>(ph) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4*>(ph + 128) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
                 *reinterpret_cast<uint4*>(ph + kPBytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -538,9 +521,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 bi::fence_proxy_async_smem();  // the weights are read by the tensor core
                 if (first) {
                     if (p > 0) {
-                        // the chunk that ended: both halves of its O are needed
-                        for (int h = 0; h < kOHalves; ++h)
-                            if (!warp_wait(&ovdone[h], (p - 1) & 1)) return false;
+                        // the chunk that ended: its O is complete once the
+                        // previous page's products are done
+                        if (!wait_products(p - 1)) return false;
                         bi::tc_fence_after();
                         fold_chunk(p / kPagesPerChunk - 1, m_prev, l_prev);
                     }
@@ -549,15 +532,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int i = 0; i < 32; ++i) z[i] = 0u;
 #pragma unroll
                     for (int q4 = 0; q4 < kD / 32; ++q4) bi::tmem_st_32x32b_x32(col_o + 32 * q4, z);
-                    for (int h = 0; h < kOHalves; ++h) hand_over(h);
-                    return true;
-                }
-                for (int h = 0; h < kOHalves; ++h) {
-                    if (!warp_wait(&ovdone[h], (p - 1) & 1)) return false;
+                } else if (__any_sync(0xffffffffu, al != 1.f)) {
+                    // alpha == 1 leaves O's bits unchanged, so only a moved
+                    // reference maximum needs O rescaled (after the previous
+                    // page's products)
+                    if (!wait_products(p - 1)) return false;
                     bi::tc_fence_after();
-                    rescale_half(h, al);
-                    hand_over(h);
+#pragma unroll 1
+                    for (int q4 = 0; q4 < kD / 32; ++q4) {
+                        uint32_t o0[32];
+                        const uint32_t cb = col_o + static_cast<uint32_t>(32 * q4);
+                        bi::tmem_ld_32x32b_x32(cb, o0);
+                        bi::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o0[i] = __float_as_uint(__fmul_rn(__uint_as_float(o0[i]), al));
+                        bi::tmem_st_32x32b_x32(cb, o0);
+                    }
                 }
+                hand_over(pb);
                 return true;
             };
 
@@ -589,8 +581,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
-            bool last_ok = ok;
-            for (int h = 0; last_ok && h < kOHalves; ++h) last_ok = warp_wait(&ovdone[h], (np - 1) & 1);
+            const bool last_ok = ok && wait_products(np - 1);
             if (last_ok) {
                 bi::tc_fence_after();
                 fold_chunk((np - 1) / kPagesPerChunk, m, l);
