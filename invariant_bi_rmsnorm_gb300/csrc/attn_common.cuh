@@ -255,4 +255,12 @@ __device__ __forceinline__ float fold_value(float acc, float fo, float part, flo
     return __fmaf_rn(part, fc, __fmul_rn(acc, fo));
 }
 
+// A column's output is its folded weighted sum of values times the
+// reciprocal of its folded weight sum: one correctly rounded reciprocal per
+// column and one rounded product per element (a division per element costs
+// several times more).  Every path normalises through these two, so decode,
+// its fold kernel and prefill round alike.
+__device__ __forceinline__ float inv_weight(float l) { return __frcp_rn(l); }
+__device__ __forceinline__ float normalise(float acc, float inv_l) { return __fmul_rn(acc, inv_l); }
+
 }  // namespace bi_attn

@@ -248,14 +248,15 @@ __device__ __forceinline__ void fold_sequence(const SplitArgs& a, int s, int g, 
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
         __nv_bfloat16* o = a.out + (row0 + h0 + j) * kD + d0;
+        const float il = bi_attn::inv_weight(Lr[j]);
         if constexpr (ND % 2 == 0) {
 #pragma unroll
             for (int e = 0; e < ND; e += 2)
                 *reinterpret_cast<__nv_bfloat162*>(o + e) = __halves2bfloat162(
-                    __float2bfloat16_rn(__fdiv_rn(A[j][e], Lr[j])),
-                    __float2bfloat16_rn(__fdiv_rn(A[j][e + 1], Lr[j])));
+                    __float2bfloat16_rn(bi_attn::normalise(A[j][e], il)),
+                    __float2bfloat16_rn(bi_attn::normalise(A[j][e + 1], il)));
         } else {
-            o[0] = __float2bfloat16_rn(__fdiv_rn(A[j][0], Lr[j]));
+            o[0] = __float2bfloat16_rn(bi_attn::normalise(A[j][0], il));
         }
     }
 }
@@ -482,7 +483,8 @@ __global__ void __launch_bounds__(kThreads)
         const int d = tid;
         for (int h = 0; h < a.group; ++h) {
             const int64_t row = static_cast<int64_t>(s) * a.Hq + g * a.group + h;
-            a.out[row * kD + d] = __float2bfloat16_rn(__fdiv_rn(fold_o[h * kD + d], fold_l[h]));
+            a.out[row * kD + d] = __float2bfloat16_rn(
+                bi_attn::normalise(fold_o[h * kD + d], bi_attn::inv_weight(fold_l[h])));
         }
         return;
     }
@@ -808,7 +810,8 @@ __global__ void __launch_bounds__(kD)
             M = Mn;
         }
     }
-    out[(static_cast<int64_t>(s) * Hq + hq) * kD + d] = __float2bfloat16_rn(__fdiv_rn(A, Ls));
+    out[(static_cast<int64_t>(s) * Hq + hq) * kD + d] =
+        __float2bfloat16_rn(bi_attn::normalise(A, bi_attn::inv_weight(Ls)));
 }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }

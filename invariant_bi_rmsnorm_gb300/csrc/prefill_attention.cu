@@ -36,8 +36,10 @@
 // of four pages and V page by page; warp 1 issues the output products and
 // warp 6 the score products, each from one thread; warps 2-5 are the softmax
 // threads, one column each (warp w reads TMEM lanes 32 (w % 4) ..).
-// O's 128 dims are handed over in two halves, so the softmax threads rescale
-// one half while the tensor core runs the other's products.  A page a row
+// A page's weights are handed to the tensor core as soon as they are
+// written; the softmax threads wait for the previous page's products only to
+// rescale O (rare: the reference maximum moves only past a slack), to fold a
+// finished chunk, or to finish the tile.  A page a row
 // cannot see leaves that row's state exactly unchanged (alpha = 1, weights
 // 0).  Rows longer than one chunk keep their running output in a caller
 // workspace between chunks.
@@ -412,6 +414,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool live = c < rpt * G && rr < nrt[t];
             const int Lc = live ? Lbase + r0 + t * rpt + rr : 0;
             const int64_t row = static_cast<int64_t>(q0 + r0 + t * rpt + rr) * a.Hq + g * G + c % G;
+            // This column's running output in the workspace.  The tile owns
+            // the workspace span of its rows' tokens ([T][Hq][D] floats in
+            // size); the kv-head's share of it is laid out dims-by-4 major,
+            // column minor, so the 32 columns of a warp move 512 contiguous
+            // bytes per access.
+            const int ncols = nrt[t] * G;
+            const int wstride = 4 * ncols;
+            float* wcol = a.ws == nullptr ? nullptr
+                                          : a.ws + static_cast<int64_t>(q0 + r0 + t * rpt) * a.Hq * kD +
+                                                static_cast<int64_t>(g) * ncols * kD + 4 * c;
             // this column's weights in the page's P operands (high parts,
             // remainders), buffer p % kPBufs
             uint8_t* p_col = smem + kOffP + (c >> 3) * 256 + (c & 7) * 16;
@@ -440,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         Mr = Mn;
                     }
                 }
-                float* wrow = a.ws + row * kD;
+                const float il = bi_attn::inv_weight(Lr);
 #pragma unroll 1
                 for (int q4 = 0; q4 < kD / 32; ++q4) {
                     uint32_t o[32];
@@ -457,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             A[i + 2] = __uint_as_float(o[i + 2]);
                             A[i + 3] = __uint_as_float(o[i + 3]);
                         } else {
-                            const float4 w = *reinterpret_cast<const float4*>(wrow + 32 * q4 + i);
+                            const float4 w = *reinterpret_cast<const float4*>(wcol + (8 * q4 + i / 4) * wstride);
                             A[i] = bi_attn::fold_value(w.x, fo, __uint_as_float(o[i]), fc);
                             A[i + 1] = bi_attn::fold_value(w.y, fo, __uint_as_float(o[i + 1]), fc);
                             A[i + 2] = bi_attn::fold_value(w.z, fo, __uint_as_float(o[i + 2]), fc);
@@ -469,16 +481,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                         for (int i = 0; i < 32; i += 8) {
                             uint4 v;
-                            v.x = bi::pack_bf16x2(__fdiv_rn(A[i], Lr), __fdiv_rn(A[i + 1], Lr));
-                            v.y = bi::pack_bf16x2(__fdiv_rn(A[i + 2], Lr), __fdiv_rn(A[i + 3], Lr));
-                            v.z = bi::pack_bf16x2(__fdiv_rn(A[i + 4], Lr), __fdiv_rn(A[i + 5], Lr));
-                            v.w = bi::pack_bf16x2(__fdiv_rn(A[i + 6], Lr), __fdiv_rn(A[i + 7], Lr));
+                            v.x = bi::pack_bf16x2(bi_attn::normalise(A[i], il), bi_attn::normalise(A[i + 1], il));
+                            v.y = bi::pack_bf16x2(bi_attn::normalise(A[i + 2], il), bi_attn::normalise(A[i + 3], il));
+                            v.z = bi::pack_bf16x2(bi_attn::normalise(A[i + 4], il), bi_attn::normalise(A[i + 5], il));
+                            v.w = bi::pack_bf16x2(bi_attn::normalise(A[i + 6], il), bi_attn::normalise(A[i + 7], il));
                             *reinterpret_cast<uint4*>(orow + i) = v;
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(wrow + 32 * q4 + i) =
+                            *reinterpret_cast<float4*>(wcol + (8 * q4 + i / 4) * wstride) =
                                 make_float4(A[i], A[i + 1], A[i + 2], A[i + 3]);
                     }
                 }
