@@ -275,8 +275,10 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
  *                its contents need no initialisation and are undefined after.
  *   S <= 65535; other arguments as bi_decode_attention.
  * Errors: as bi_decode_attention; an inconsistent q_indptr / seq_lens entry
- * or an out-of-range page is reported on the device (BI_ERR_DEVICE_BAD_INPUT)
- * and the affected sequence is skipped.
+ * is reported on the device (BI_ERR_DEVICE_BAD_INPUT) and the sequence is
+ * skipped; an out-of-range page is reported the same way, is read as zeros
+ * (no fault), and the 128-column query tiles whose rows reach it are not
+ * written (the sequence's other rows are).
  */
 bi_status bi_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_table, int32_t max_pages_per_seq,

@@ -211,7 +211,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* pfull = sfree + kTiles * kSBuf;    // [kPBufs] a page's weights written (O ready)
     uint64_t* pempty = pfull + kPBufs;           // [kPBufs] that page's products done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + kPBufs);
-    __shared__ int bad_page;
     if (tid == 0) {
         for (int i = 0; i < kKSlots; ++i) {
             bi::mbar_init(&kfull[i], 1);
@@ -236,9 +235,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         bi::tma_prefetch_desc(&tmap_q);
         bi::tma_prefetch_desc(&tmap_k);
         bi::tma_prefetch_desc(&tmap_v);
-        bad_page = 0;
-        // the Q tile does not depend on the page table: its loads go out
-        // now, overlapping the page-table check below
+        // the Q tile does not depend on the page table: its loads go out now
         const uint32_t qbytes = static_cast<uint32_t>(ntiles * 2 * 64 * G * rpt * 2);
         bi::mbar_arrive_expect_tx(qfull, qbytes);
         for (int t = 0; t < ntiles; ++t)
@@ -251,19 +248,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         bi::tmem_relinquish();
     }
     const int32_t* bt = a.block_table + static_cast<int64_t>(s) * a.max_pages_per_seq;
-    __syncthreads();
-    for (int i = tid; i < npg; i += kThreads) {
-        const int pg = bt[i];
-        if (pg < 0 || pg >= a.num_pages) bad_page = 1;
-    }
     bi::tc_fence_before();
     __syncthreads();
     bi::tc_fence_after();
     const uint32_t tm = *tmem_slot;
-    if (bad_page && tid == 0) bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
-    const bool work = !bad_page;
+    // The page table is not checked before the loads go out: a page outside
+    // the cache maps past the tensor's end, where a TMA load reads zeros, and
+    // the softmax threads judge the pages before they write anything.
+    auto page_row = [&](int pg) -> int32_t {
+        if (pg < 0 || pg >= a.num_pages) return a.num_pages * a.Hkv * kPage;
+        return (pg * a.Hkv + g) * kPage;
+    };
 
-    if (work && warp == 0) {
+    if (warp == 0) {
         // ---------------- producers: lane 0 the Q tiles and the K blocks,
         // lane 16 the V pages (independent loops, each on its own ring) ------
         if (lane == 0) {
@@ -278,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint8_t* kd = smem + kOffK + slot * kKSlotBytes;
                 bi::mbar_arrive_expect_tx(&kfull[slot], static_cast<uint32_t>(np * 2 * kHalfBytes));
                 for (int j = 0; j < np; ++j) {
-                    const int row = (bt[b * kGroupPages + j] * a.Hkv + g) * kPage;
+                    const int32_t row = page_row(bt[b * kGroupPages + j]);
                     bi::tma_load_2d(kd + j * kHalfBytes, &tmap_k, &kfull[slot], 0, row);
                     bi::tma_load_2d(kd + kGroupPages * kHalfBytes + j * kHalfBytes, &tmap_k,
                                     &kfull[slot], 64, row);
@@ -297,14 +294,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                     bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
                     break;
                 }
-                const int row = (bt[p] * a.Hkv + g) * kPage;
+                const int32_t row = page_row(bt[p]);
                 bi::mbar_arrive_expect_tx(&vfull[slot], kMatBytes);
                 bi::tma_load_3d(smem + kOffV + slot * kMatBytes, &tmap_v, &vfull[slot], 0, row, 0);
             }
             for (int i = max(0, p - kVSlots); i < p; ++i)
                 bi::mbar_wait_for(&vfull[i % kVSlots], (i / kVSlots) & 1, bi::kDrainNs);
         }
-    } else if (work && warp == 1) {
+    } else if (warp == 1) {
         // ---------------- output products (lane 0 issues; the warp waits
         // together).  The descriptors are built before the waits: the start
         // address field is addr >> 4, so a shared-memory offset is added as
@@ -360,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             __syncwarp();
         }
-    } else if (work && warp == kScoreWarp) {
+    } else if (warp == kScoreWarp) {
         // ---------------- score products (lane 0 issues), on their own
         // thread so that no output product queues behind them: block b of
         // four pages into TMEM buffer b % kSBuf once its K block has landed
@@ -402,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             __syncwarp();
         }
-    } else if (work && warp >= 2) {
+    } else if (warp >= 2) {
         // ---------------- softmax: thread = one (row, head) column -----------
         const int t = (warp - 2) / kSoftWarps;
         if (t < ntiles) {
@@ -430,6 +427,22 @@ __global__ void __launch_bounds__(kThreads, 2)
             float m = -INFINITY, l = 0.f;    // online softmax of the current chunk
             float Mr = -INFINITY, Lr = 0.f;  // fold over the finished chunks
             bool ok = true;
+            // A page outside the cache: the tile is computed on the zeros its
+            // loads read there and is not written.  The page numbers are read
+            // now and judged at the first write, so the loads' latency hides
+            // behind the tile's pages.
+            const int pg0 = lane < npg ? bt[lane] : 0;
+            int bad_more = 0;
+            for (int i = lane + 32; i < npg; i += 32) bad_more |= bt[i] < 0 || bt[i] >= a.num_pages;
+            int judged = 0;
+            bool writes = true;
+            auto judge = [&]() {
+                if (judged) return;
+                judged = 1;
+                writes = !__any_sync(0xffffffffu, pg0 < 0 || pg0 >= a.num_pages || bad_more);
+                if (!writes && warp == 2 && lane == 0)
+                    bi::report_error(a.err, bi::kErrBadInput | bi::kWhereAttnSplit);
+            };
 
             // Fold chunk k (state mk, lk and its O in TMEM) into the column's
             // running state, as decode folds a chunk partial, and write the
@@ -438,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // workspace between chunks.  Columns that do not see chunk k are
             // left unchanged.
             auto fold_chunk = [&](int k, float mk, float lk) {
+                judge();
                 const bool sees = Lc > k * kChunk;
                 const bool last = sees && Lc <= (k + 1) * kChunk;
                 float fo = 1.f, fc = 1.f;
@@ -459,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     __syncwarp();
                     bi::tmem_ld_32x32b_x32(col_o + 32 * q4, o);
                     bi::tmem_ld_wait();
-                    if (!sees) continue;
+                    if (!sees || !writes) continue;
                     float A[32];
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
@@ -603,9 +617,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
 
-    // a CTA that skipped its work still has the Q copies issued at set-up in
-    // flight: its shared memory outlives them (bounded wait)
-    if (!work && tid == 0) bi::mbar_wait_for(qfull, 0, bi::kDrainNs);
     bi::tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -137,3 +137,28 @@ def test_inconsistent_indptr_reported_without_fault():
     with pytest.raises(bi.BiError, match="BAD_INPUT"):
         bi.get_device_error()
     bi.get_device_error()
+
+
+def test_page_outside_the_cache_reported_and_only_its_readers_skipped():
+    # a 100-token prompt in tiles of 32 rows: rows 0-31 read pages 0-1,
+    # rows 96-99 read pages 0-6.  Page 6 (tokens 96-99) points past the
+    # cache: the tile that reads it is reported and not written (its loads
+    # read zeros there, no fault); every other tile keeps its clean bits.
+    lens = [100]
+    p, q = _prompts(lens, seed=460)
+    clean = bits(_prefill(p, q, lens))
+    bad = {k: v.clone() for k, v in p.items()}
+    bad["block_table"][0, 6] = int(p["k_cache"].shape[0]) + 5
+    bi.get_device_error()
+    sentinel = torch.full((100, 32, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    d = {k: v.cuda() for k, v in bad.items()}
+    indptr = torch.tensor([0, 100], dtype=torch.int32, device="cuda")
+    out = bi.prefill_attention(q.cuda(), d["k_cache"], d["v_cache"], d["block_table"],
+                               d["seq_lens"], indptr, max_q_len=100, max_seq_len=100,
+                               out=sentinel)
+    with pytest.raises(bi.BiError, match="BAD_INPUT"):
+        bi.get_device_error()
+    bi.get_device_error()
+    got = bits(out)
+    assert np.array_equal(got[:96], clean[:96])
+    assert (got[96:] == bits(torch.full((4, 32, 128), 7.0, dtype=torch.bfloat16))).all()
