@@ -42,53 +42,62 @@ struct RopeArgs {
     uint32_t* err;
 };
 
-// One CTA of 8 warps per token; warp w takes heads w, w+8, w+16, ... and
-// issues the loads of up to kHeadsPerPass of them before computing any, so
-// enough bytes are in flight to cover HBM latency.  Per head, lane l holds
-// dims 2l, 2l+1 (first half) and 64+2l, 64+2l+1 (their rotation partners):
+// One CTA of 8 warps per token.  A warp works on two heads at once, one per
+// half-warp: warp w takes head pairs w, w+8, w+16 (heads 2p and 2p+1) and
+// issues the loads of all its pairs before computing any, so enough bytes
+// are in flight to cover HBM latency.  Per head, lane l of its half (l =
+// lane & 15) holds dims 4l .. 4l+3 and their rotation partners 64+4l ..
+// 64+4l+3:
 //   q, k heads:  x -> bf16(x * rsqrt(mean(x^2) + eps) * w)   (if a norm weight is given;
-//                    sum of squares: per lane in the order 2l, 2l+1, 64+2l, 64+2l+1, then
-//                    an xor butterfly over lanes)
+//                    sum of squares: per lane in the order 4l .. 4l+3, 64+4l .. 64+4l+3,
+//                    then an xor butterfly over the 16 lanes of the half, strides 8, 4, 2, 1)
 //                -> rotate-half RoPE in fp32: y_i = x_i c_i - x_{64+i} s_i,
 //                   y_{64+i} = x_{64+i} c_i + x_i s_i, rounded once to bf16
 //   v heads:     copied.
 // q goes to q_out; k and v to their token's cache slot.  Each head's
 // arithmetic depends only on its own 128 values, the position and the weights.
 constexpr int kRopeWarps = 8;
-constexpr int kHeadsPerPass = 6;
+constexpr int kPairsPerPass = 3;
 
-__device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
-    return *reinterpret_cast<const uint32_t*>(p);
+__device__ __forceinline__ uint2 ld_b64(const __nv_bfloat16* p) {
+    return *reinterpret_cast<const uint2*>(p);
 }
 
-__device__ __forceinline__ void load_heads(const __nv_bfloat16* row, int h0, int heads, int i0,
-                                           uint32_t (&lo)[kHeadsPerPass],
-                                           uint32_t (&hi)[kHeadsPerPass]) {
+__device__ __forceinline__ void load_pairs(const __nv_bfloat16* row, int p0, int heads, int half,
+                                           int i0, uint2 (&lo)[kPairsPerPass],
+                                           uint2 (&hi)[kPairsPerPass]) {
 #pragma unroll
-    for (int j = 0; j < kHeadsPerPass; ++j) {
-        const int h = h0 + j * kRopeWarps;
+    for (int j = 0; j < kPairsPerPass; ++j) {
+        const int h = 2 * (p0 + j * kRopeWarps) + half;
         if (h < heads) {
-            lo[j] = ld_b32(row + static_cast<int64_t>(h) * kD + i0);
-            hi[j] = ld_b32(row + static_cast<int64_t>(h) * kD + kHalf + i0);
+            lo[j] = ld_b64(row + static_cast<int64_t>(h) * kD + i0);
+            hi[j] = ld_b64(row + static_cast<int64_t>(h) * kD + kHalf + i0);
         }
     }
 }
 
-// six CTAs (48 warps) per SM: capping registers at 40 ran 10 % faster than the
-// natural 61 (four CTAs); at 32 the spills cost more than the extra CTAs gave
-__global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel(const RopeArgs a) {
+__device__ __forceinline__ void unpack4(uint2 v, float* x) {
+    x[0] = __uint_as_float(v.x << 16);
+    x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16);
+    x[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+
+__global__ void __launch_bounds__(kRopeWarps * 32, 4) qk_norm_rope_append_kernel(const RopeArgs a) {
     bi::launch_dependents();
     bi::grid_dependency_wait();  // nothing global is touched before the previous kernel ends
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int half = lane >> 4;
     const int heads = a.Hq + 2 * a.Hkv;
-    const int i0 = 2 * lane;
+    const int pairs = (heads + 1) / 2;
+    const int i0 = 4 * (lane & 15);
     const __nv_bfloat16* row = a.qkv + static_cast<int64_t>(t) * a.ld_qkv;
     // the first pass's q/k/v loads go out before the position is known, so
     // their latency overlaps that of the position -> RoPE-table chain
-    uint32_t lo[kHeadsPerPass], hi[kHeadsPerPass];
-    load_heads(row, warp, heads, i0, lo, hi);
+    uint2 lo[kPairsPerPass], hi[kPairsPerPass];
+    load_pairs(row, warp, heads, half, i0, lo, hi);
     const int pos = a.positions[t];
     const int64_t slot = a.slots[t];
     if (pos < 0 || pos >= a.max_pos || slot < 0 || slot >= a.num_slots) {
@@ -96,54 +105,63 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
         return;
     }
     const float* cs = a.rope + static_cast<int64_t>(pos) * kD;
-    const float2 cosv = *reinterpret_cast<const float2*>(cs + i0);
-    const float2 sinv = *reinterpret_cast<const float2*>(cs + kHalf + i0);
-    const float c[2] = {cosv.x, cosv.y}, sn[2] = {sinv.x, sinv.y};
-    const int idx[4] = {i0, i0 + 1, kHalf + i0, kHalf + i0 + 1};
-    float qw[4], kw[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        qw[e] = a.q_norm_w ? bf(a.q_norm_w[idx[e]]) : 0.f;
-        kw[e] = a.k_norm_w ? bf(a.k_norm_w[idx[e]]) : 0.f;
-    }
+    const float4 cosv = *reinterpret_cast<const float4*>(cs + i0);
+    const float4 sinv = *reinterpret_cast<const float4*>(cs + kHalf + i0);
+    const float c[4] = {cosv.x, cosv.y, cosv.z, cosv.w};
+    const float sn[4] = {sinv.x, sinv.y, sinv.z, sinv.w};
+    // the norm weights of this lane's 8 dims, as bf16 pairs (unpacked where used)
+    const uint2 zero2 = make_uint2(0u, 0u);
+    const uint2 qw_lo = a.q_norm_w ? ld_b64(a.q_norm_w + i0) : zero2;
+    const uint2 qw_hi = a.q_norm_w ? ld_b64(a.q_norm_w + kHalf + i0) : zero2;
+    const uint2 kw_lo = a.k_norm_w ? ld_b64(a.k_norm_w + i0) : zero2;
+    const uint2 kw_hi = a.k_norm_w ? ld_b64(a.k_norm_w + kHalf + i0) : zero2;
     // the token's slot in every kv-head's page block (page size fixed at BI_PAGE_SIZE)
     const int64_t page = slot / BI_PAGE_SIZE, off = slot % BI_PAGE_SIZE;
     const int64_t kv_slot = (page * a.Hkv * BI_PAGE_SIZE + off) * kD;
 
-    for (int h0 = warp; h0 < heads; h0 += kRopeWarps * kHeadsPerPass) {
-        if (h0 != warp) load_heads(row, h0, heads, i0, lo, hi);
+    for (int p0 = warp; p0 < pairs; p0 += kRopeWarps * kPairsPerPass) {
+        if (p0 != warp) load_pairs(row, p0, heads, half, i0, lo, hi);
 #pragma unroll
-        for (int j = 0; j < kHeadsPerPass; ++j) {
-            const int h = h0 + j * kRopeWarps;  // the same for every lane
-            if (h >= heads) break;
-            if (h >= a.Hq + a.Hkv) {  // v: copy into the cache
+        for (int j = 0; j < kPairsPerPass; ++j) {
+            const int pr = p0 + j * kRopeWarps;  // the same for every lane
+            if (pr >= pairs) break;
+            const int h = 2 * pr + half;        // this half's head
+            const bool live = h < heads;
+            const bool is_v = h >= a.Hq + a.Hkv;
+            const bool is_q = h < a.Hq;
+            float x[8];
+            unpack4(lo[j], x);
+            unpack4(hi[j], x + 4);
+            // every lane takes part in the butterfly (both halves, any head kind)
+            const bool norm = is_q ? a.q_norm_w != nullptr : a.k_norm_w != nullptr;
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (!live) continue;
+            if (is_v) {  // v: copy into the cache
                 const int hv = h - a.Hq - a.Hkv;
                 __nv_bfloat16* dst = a.v_cache + kv_slot + hv * (BI_PAGE_SIZE * kD);
-                *reinterpret_cast<uint32_t*>(dst + i0) = lo[j];
-                *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = hi[j];
+                *reinterpret_cast<uint2*>(dst + i0) = lo[j];
+                *reinterpret_cast<uint2*>(dst + kHalf + i0) = hi[j];
                 continue;
             }
-            float x[4] = {__uint_as_float(lo[j] << 16), __uint_as_float(lo[j] & 0xffff0000u),
-                          __uint_as_float(hi[j] << 16), __uint_as_float(hi[j] & 0xffff0000u)};
-            const bool is_q = h < a.Hq;
-            if (is_q ? a.q_norm_w != nullptr : a.k_norm_w != nullptr) {
-                float ss = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) ss = __fmaf_rn(x[e], x[e], ss);
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (norm) {
                 // ss / 128 computed as ss * 2^-7: the same correctly rounded value
                 const float r = rsqrtf(__fmul_rn(ss, 1.f / kD) + a.eps);
+                float w[8];
+                unpack4(is_q ? qw_lo : kw_lo, w);
+                unpack4(is_q ? qw_hi : kw_hi, w + 4);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    x[e] = __bfloat162float(
-                        __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[e], r), is_q ? qw[e] : kw[e])));
+                for (int e = 0; e < 8; ++e)
+                    x[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(x[e], r), w[e])));
             }
-            float y[4];
+            float y[8];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                y[e] = __fsub_rn(__fmul_rn(x[e], c[e]), __fmul_rn(x[2 + e], sn[e]));
-                y[2 + e] = __fadd_rn(__fmul_rn(x[2 + e], c[e]), __fmul_rn(x[e], sn[e]));
+            for (int e = 0; e < 4; ++e) {
+                y[e] = __fsub_rn(__fmul_rn(x[e], c[e]), __fmul_rn(x[4 + e], sn[e]));
+                y[4 + e] = __fadd_rn(__fmul_rn(x[4 + e], c[e]), __fmul_rn(x[e], sn[e]));
             }
             __nv_bfloat16* dst;
             if (is_q) {
@@ -151,8 +169,10 @@ __global__ void __launch_bounds__(kRopeWarps * 32, 6) qk_norm_rope_append_kernel
             } else {
                 dst = a.k_cache + kv_slot + (h - a.Hq) * (BI_PAGE_SIZE * kD);
             }
-            *reinterpret_cast<uint32_t*>(dst + i0) = bi::pack_bf16x2(y[0], y[1]);
-            *reinterpret_cast<uint32_t*>(dst + kHalf + i0) = bi::pack_bf16x2(y[2], y[3]);
+            *reinterpret_cast<uint2*>(dst + i0) =
+                make_uint2(bi::pack_bf16x2(y[0], y[1]), bi::pack_bf16x2(y[2], y[3]));
+            *reinterpret_cast<uint2*>(dst + kHalf + i0) =
+                make_uint2(bi::pack_bf16x2(y[4], y[5]), bi::pack_bf16x2(y[6], y[7]));
         }
     }
 }
