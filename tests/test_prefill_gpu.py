@@ -162,3 +162,28 @@ def test_page_outside_the_cache_reported_and_only_its_readers_skipped():
     got = bits(out)
     assert np.array_equal(got[:96], clean[:96])
     assert (got[96:] == bits(torch.full((4, 32, 128), 7.0, dtype=torch.bfloat16))).all()
+
+
+def test_bench_workload_every_row_equals_decode():
+    # the launch the bench times: 29 prompts of U[32, 512] tokens (8048 rows,
+    # 3712 CTAs, most tile classes and the empty ones); every row against
+    # decode bit for bit, a sample against the oracle
+    lens_all = inputs.seq_lens_uniform(64, 512, seed=610, min_len=32).tolist()
+    lens, tot = [], 0
+    for L in lens_all:
+        if tot + L > 8192:
+            break
+        lens.append(L)
+        tot += L
+    p = inputs.decode_problem(len(lens), Hq=32, Hkv=8, D=128, seq_lens=lens, seed=611)
+    q = inputs.normal_bf16((tot, 32, 128), 612)
+    out = _prefill(p, q, lens)
+    rows = [(i, r + 1) for i, L in enumerate(lens) for r in range(L)]
+    e = _expanded(p, q, rows)
+    dec = bi.decode_attention(e["q"].cuda(), e["k_cache"].cuda(), e["v_cache"].cuda(),
+                              e["block_table"].cuda(), e["seq_lens"].cuda(), max_seq_len=max(lens))
+    same = (bits(out) == bits(dec)).all(axis=(1, 2))
+    assert same.all(), f"{(~same).sum()} of {len(rows)} rows differ from decode; first {np.argmin(same)}"
+    pick = np.unique(np.r_[0:8, np.linspace(0, tot - 1, 56).astype(int)])
+    sub = _expanded(p, q[torch.from_numpy(pick)], [rows[i] for i in pick])
+    _check(out[torch.from_numpy(pick).cuda()], oracle.decode_attention(**sub))
