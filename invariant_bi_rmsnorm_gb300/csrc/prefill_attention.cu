@@ -72,14 +72,10 @@ constexpr int kThreads = (kScoreWarp + 1) * 32;
 constexpr int kGroupPages = 4;   // pages per score block: S is one N = 64 product
 constexpr int kKSlots = 2;       // K ring, in score blocks
 constexpr int kKSlotBytes = 2 * kGroupPages * kHalfBytes;  // [dim half][64 tokens][128 B]: 16 KB
-constexpr int kVSlots = 4;       // V ring, in pages
 constexpr int kSBuf = 2;         // score blocks per tile in TMEM
 constexpr int kQHalf = kCols * 128;          // one 64-dim half of a Q tile: 16 KB
 constexpr int kQBytes = 2 * kQHalf;          // 32 KB
 constexpr int kPBytes = kCols * kPage * 2;   // one bf16 [128][16] weight operand: 4 KB
-constexpr int kOffK = kTiles * kQBytes;
-constexpr int kOffV = kOffK + kKSlots * kKSlotBytes;
-constexpr int kOffP = kOffV + kVSlots * kMatBytes;
 // Weight operands by page.  A page is handed to the tensor core as soon as
 // its weights are written: its products add onto O behind the previous
 // page's in the tensor pipe, so the softmax threads wait for the previous
@@ -87,8 +83,15 @@ constexpr int kOffP = kOffV + kVSlots * kMatBytes;
 // the reference-maximum slack makes rare, a chunk fold, the tile's end).
 // The buffers bound how far ahead of the tensor core they run.
 constexpr int kPBufs = 3;
+// V ring, in pages, one slot per weight buffer: page p's V slot and weight
+// buffer are free again once page p's products are done (pempty), so one
+// barrier per slot serves both rings and the output products need one commit.
+constexpr int kVSlots = kPBufs;
+constexpr int kOffK = kTiles * kQBytes;
+constexpr int kOffV = kOffK + kKSlots * kKSlotBytes;
+constexpr int kOffP = kOffV + kVSlots * kMatBytes;
 constexpr int kOffBar = kOffP + kPBufs * 2 * kPBytes;
-constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 3 + 2 * kSBuf + 2 * kPBufs;
+constexpr int kNumBars = 2 * kKSlots + kVSlots + 3 + 2 * kSBuf + 2 * kPBufs;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024 /*align*/;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // TMEM columns: O of tile t at t * 128; score block b of tile t at kColS +
@@ -202,8 +205,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kOffBar);  // [kKSlots] K block landed
     uint64_t* kempty = kfull + kKSlots;                              // [kKSlots] K slot free
     uint64_t* vfull = kempty + kKSlots;                              // [kVSlots] V page landed
-    uint64_t* vempty = vfull + kVSlots;                              // [kVSlots] V slot free
-    uint64_t* qfull = vempty + kVSlots;                              // Q tiles landed
+    uint64_t* qfull = vfull + kVSlots;                               // Q tiles landed
     uint64_t* drain = qfull + 1;                                     // output MMAs after a timeout
     uint64_t* drain_s = drain + 1;                                   // score MMAs after a timeout
     uint64_t* sfull = drain_s + 1;               // [kTiles][kSBuf] score block ready
@@ -218,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         for (int i = 0; i < kVSlots; ++i) {
             bi::mbar_init(&vfull[i], 1);
-            bi::mbar_init(&vempty[i], 1);
         }
         bi::mbar_init(qfull, 1);
         bi::mbar_init(drain, 1);
@@ -290,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             int p = 0;
             for (; p < npg; ++p) {
                 const int slot = p % kVSlots;
-                if (!bi::mbar_wait(&vempty[slot], ((p / kVSlots) & 1) ^ 1)) {
+                // the slot's previous page (p - kVSlots) has had its products
+                if (!bi::mbar_wait(&pempty[slot], ((p / kVSlots) & 1) ^ 1)) {
                     bi::report_error(a.err, bi::kErrTimeout | bi::kWhereAttnSplit);
                     break;
                 }
@@ -340,9 +342,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 bi::tc_commit(&pempty[pb]);  // the page's products (and all before) done
             }
             issued = true;
-            __syncwarp();
-            if (!ok) break;
-            if (lane == 0) bi::tc_commit(&vempty[vslot]);
             __syncwarp();
         }
         if (!ok) {
