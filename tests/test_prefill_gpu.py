@@ -187,3 +187,31 @@ def test_bench_workload_every_row_equals_decode():
     pick = np.unique(np.r_[0:8, np.linspace(0, tot - 1, 56).astype(int)])
     sub = _expanded(p, q[torch.from_numpy(pick)], [rows[i] for i in pick])
     _check(out[torch.from_numpy(pick).cuda()], oracle.decode_attention(**sub))
+
+
+@pytest.mark.parametrize("kind", ["flat", "peaked", "ramp"])
+def test_adversarial_scores_match_decode_bitwise(kind):
+    # flat: q = 0, every score equal; peaked: q x 40, a nearly one-hot
+    # softmax; ramp: page j of each prompt holds K x (1 + j), so the scores
+    # grow along the prompt and the reference maximum keeps moving past its
+    # slack -- the path that rescales O in TMEM, which seeded N(0, 1) data
+    # almost never takes
+    lens = [300, 700]
+    p, q = _prompts(lens, seed=470)
+    if kind == "flat":
+        q = torch.zeros_like(q)
+    elif kind == "peaked":
+        q = (q.float() * 40.0).to(torch.bfloat16)
+    else:
+        for s, L in enumerate(lens):
+            for j in range((L + 15) // 16):
+                pg = int(p["block_table"][s, j])
+                p["k_cache"][pg] = (p["k_cache"][pg].float() * (1.0 + j)).to(torch.bfloat16)
+    out = _prefill(p, q, lens)
+    rows = [(i, r + 1) for i, L in enumerate(lens) for r in range(L)]
+    e = _expanded(p, q, rows)
+    dec = bi.decode_attention(e["q"].cuda(), e["k_cache"].cuda(), e["v_cache"].cuda(),
+                              e["block_table"].cuda(), e["seq_lens"].cuda(), max_seq_len=max(lens))
+    same = (bits(out) == bits(dec)).all(axis=(1, 2))
+    assert same.all(), f"{(~same).sum()} of {len(rows)} rows differ from decode; first {np.argmin(same)}"
+    _check(out, oracle.decode_attention(**e))
