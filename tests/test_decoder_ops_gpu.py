@@ -50,8 +50,11 @@ def test_silu_mul_against_oracle():
     assert ulp_distance(out, ref).max() <= 2
 
 
-def test_qk_norm_rope_append_against_oracle():
-    T, Hq, Hkv, D = 37, 32, 8, 128
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (3, 1), (12, 3), (5, 5), (64, 8)])
+def test_qk_norm_rope_append_against_oracle(Hq, Hkv):
+    # a warp works on two heads at once: odd head counts leave a pair with
+    # one head, and pairs straddle the q/k and k/v boundaries
+    T, D = 37, 128
     qkv = inputs.normal_bf16((T, (Hq + 2 * Hkv) * D), seed=720, std=1.5)
     qn = inputs.rmsnorm_weight(D, seed=721)
     kn = inputs.rmsnorm_weight(D, seed=722)
